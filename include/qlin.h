@@ -1,0 +1,157 @@
+/*
+ * qlin.h -- C ABI of libqlin: fused affine dequantise-into-matmul for
+ * MLX-style packed 4/8-bit weights on NVIDIA GB300 (sm_103a).
+ *
+ * What the calls compute (the web pages the method comes from are cited by
+ * title and section):
+ *
+ *   Packed weight format -- "epic: realize low-precision / quantized
+ *   performance on the OpenXLA (IREE) backend", section Context: MLX 4/8-bit
+ *   weights stay resident packed as a ui32 payload with one f16 (or, per
+ *   "track(upstream-iree): fused dequant->matmul for the packed int8
+ *   bandwidth win", section "What is already in-tree", bf16) scale and bias
+ *   per group along K.
+ *
+ *   Reconstruction -- same section: bit-unpack, then w = q*scale + bias.
+ *
+ *   Fusion -- "track(upstream-iree): ...", section "The blocker (measured)":
+ *   the matmul consumes the reconstructed weight; it is never written to DRAM.
+ *
+ *   M = 1 with N not a multiple of 4 -- "Metal backend: import qmv_impl from
+ *   MLX": any N >= 1 is accepted.
+ *
+ * Shared notation and layouts (all row-major, all pointers are DEVICE
+ * pointers owned by the caller; the library never allocates or frees):
+ *
+ *   bits        4 or 8; p = 32/bits codes per uint32 word
+ *   group_size  64 (the only group size the kernels take; others return
+ *               QLIN_ERR_UNSUPPORTED)
+ *   W           N x K weights (output features x input features)
+ *   wq          uint32 [N][K/p]; code k of row n sits at bits
+ *               [bits*(k%p), bits*(k%p)+bits) of word wq[n][k/p]
+ *               ("low bits first")
+ *   scales,
+ *   biases      sdtype [N][K/group_size]
+ *   x           dtype [M][K]  (activations)
+ *   y           dtype [M][N]  (y = x . W_hat^T, f32 accumulation, one
+ *               round-to-nearest-even to dtype at the end)
+ *
+ * Errors: every call validates its arguments on the host before anything is
+ * launched and returns a status; on failure nothing was launched and
+ * qlin_last_error() (per calling thread) describes why.  A launch failure
+ * reported by the CUDA runtime returns QLIN_ERR_CUDA.  Calls are asynchronous
+ * on the given stream (a cudaStream_t passed as void*; NULL = legacy default
+ * stream) and never synchronise the device.
+ *
+ * Device-side waits in the kernels are bounded; if one gives up it sets a
+ * device status word that qlin_device_status() reads (and clears).
+ */
+#ifndef QLIN_H_
+#define QLIN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QLIN_OK = 0,
+  QLIN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, K % group_size != 0, ... */
+  QLIN_ERR_UNSUPPORTED = 2,  /* bits not in {4,8}, group_size != 64, dtype combination */
+  QLIN_ERR_MISALIGNED = 3,   /* a pointer the 128-bit / TMA path needs 16-byte aligned is not */
+  QLIN_ERR_CUDA = 4,         /* the CUDA runtime reported an error (see qlin_last_error) */
+  QLIN_ERR_DEVICE_TIMEOUT = 5 /* a kernel's bounded wait gave up (qlin_device_status) */
+} qlin_status;
+
+typedef enum { QLIN_F32 = 0, QLIN_F16 = 1, QLIN_BF16 = 2 } qlin_dtype;
+
+/* Human-readable name of a status code (static string). */
+const char* qlin_status_str(qlin_status s);
+
+/* Detail of the last failing call made by this thread (static per-thread
+ * buffer; empty string if none). */
+const char* qlin_last_error(void);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int qlin_version(void);
+
+/*
+ * Affine quantisation (load time; not on the per-token path).
+ *   w       device float32 [N][K], finite values
+ *   wq      device uint32 [N][K*bits/32]          (written)
+ *   scales,
+ *   biases  device sdtype [N][K/group_size]         (written)
+ * Per row and group G of group_size consecutive k:
+ *   scale = RNE_sdtype(fl32((max_G - min_G) / (2^bits - 1))),
+ *   bias  = RNE_sdtype(min_G),
+ *   q_k   = clamp(rint(fl32(fl32(w_k - bias) / scale)), 0, 2^bits - 1)
+ *   (ties to even; q = 0 when the stored scale is 0).
+ * The recipe is MLX's affine min/max quantisation with the rounding choices
+ * spelled out (the pages give the format, not the quantiser).
+ * sdtype: QLIN_F16 or QLIN_BF16.  Alignment: w and wq 16-byte aligned.
+ */
+qlin_status qlin_quantize_affine(const float* w, int64_t N, int64_t K, int bits, int group_size,
+                                 qlin_dtype sdtype, uint32_t* wq, void* scales, void* biases,
+                                 void* stream);
+
+/*
+ * Materialise the reconstruction w_hat[N][K] = RNE_out(q*scale + bias): one
+ * correctly rounded step from the exact value, so it is bit-identical to a
+ * host dequantisation ("What is already in-tree": in-graph reconstruction is
+ * bit-identical to the host dequant).  out_dtype: QLIN_F32, or equal to
+ * sdtype.  This is the unfused reference path and a test carrier; the matmul
+ * entry points below never call it.  Alignment: wq and w_out 16-byte aligned.
+ */
+qlin_status qlin_dequant(const uint32_t* wq, const void* scales, const void* biases, int64_t N,
+                         int64_t K, int bits, int group_size, qlin_dtype sdtype,
+                         qlin_dtype out_dtype, void* w_out, void* stream);
+
+/*
+ * Fused matrix-vector / small-M product on CUDA cores (decode):
+ *   y[m][n] = sum_k x[m][k] * (q[n][k]*scale[n][k/g] + bias[n][k/g])
+ * for m < M, n < N.  dtype (QLIN_F16 or QLIN_BF16) is the type of x, y,
+ * scales and biases.  Correct for any M >= 1 and N >= 1 (N need not be a
+ * multiple of 4); fastest for M <= 4.  Alignment: x and wq 16-byte aligned.
+ * Streams each packed word, scale and bias once per M-tile of 4 rows of x.
+ */
+qlin_status qlin_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                     void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                     qlin_dtype dtype, void* stream);
+
+/*
+ * The same product on the tensor cores (batched decode and prefill): packed
+ * tiles are staged into shared memory by TMA, dequantised there to dtype
+ * (bit-identical to qlin_dequant's dtype output) and fed to tcgen05 MMA with
+ * f32 accumulators in tensor memory.  Same arguments and result contract as
+ * qlin_qmv.  Extra requirement: K % 64 == 0 (always true for group 64) and
+ * x, wq 16-byte aligned.
+ */
+qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                     void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                     qlin_dtype dtype, void* stream);
+
+/*
+ * Dispatch to qlin_qmv when M < qlin_crossover_m(N, K, bits), else qlin_qmm.
+ */
+qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
+                        const void* biases, void* y, int64_t M, int64_t N, int64_t K, int bits,
+                        int group_size, qlin_dtype dtype, void* stream);
+
+/* Smallest M for which qlin_linear picks the tensor-core path (measured). */
+int64_t qlin_crossover_m(int64_t N, int64_t K, int bits);
+
+/*
+ * Read and clear the device status word of the current device (synchronises
+ * the device).  *flags receives 0 when no kernel gave up a bounded wait since
+ * the last call, else a bit mask of the waits that gave up.  Returns QLIN_OK,
+ * or QLIN_ERR_CUDA if the device could not be read.
+ */
+qlin_status qlin_device_status(int* flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLIN_H_ */

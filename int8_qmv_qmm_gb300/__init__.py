@@ -1,0 +1,170 @@
+"""Fused affine-dequantise-into-matmul for MLX-style packed 4/8-bit weights on
+GB300 (sm_103a).
+
+This package is a thin ctypes binding over the C ABI of ``libqlin.so``
+(declared in ``include/qlin.h``): it checks tensor placement and shape,
+allocates outputs with PyTorch and passes raw device pointers and the current
+CUDA stream.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback -- if the library is missing the
+calls raise.
+
+Layouts (row-major): packed weights ``wq`` uint32 [N, K*bits/32] (codes low
+bits first), ``scales``/``biases`` [N, K/64] in the activation dtype,
+activations ``x`` [M, K], output ``y`` [M, N].
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build_lib import LIB_PATH
+
+__all__ = [
+    "QlinError", "lib", "quantize_affine", "dequant", "qmv", "qmm", "linear",
+    "crossover_m", "device_status", "QLIN_F32", "QLIN_F16", "QLIN_BF16",
+]
+
+QLIN_F32, QLIN_F16, QLIN_BF16 = 0, 1, 2
+_DTYPE_CODE = {torch.float32: QLIN_F32, torch.float16: QLIN_F16, torch.bfloat16: QLIN_BF16}
+GROUP_SIZE = 64
+
+_c_i64, _c_int, _c_vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+
+# name -> (restype, argtypes); names match include/qlin.h
+_SIGNATURES = {
+    "qlin_status_str": (ctypes.c_char_p, [_c_int]),
+    "qlin_last_error": (ctypes.c_char_p, []),
+    "qlin_version": (_c_int, []),
+    "qlin_quantize_affine": (_c_int, [_c_vp, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_vp, _c_vp,
+                                      _c_vp, _c_vp]),
+    "qlin_dequant": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int,
+                              _c_vp, _c_vp]),
+    "qlin_qmv": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
+    "qlin_qmm": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
+    "qlin_linear": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
+    "qlin_crossover_m": (_c_i64, [_c_i64, _c_i64, _c_int]),
+    "qlin_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
+}
+
+_LIB = None
+
+
+class QlinError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(detail)
+
+
+def lib(path: str | None = None):
+    """The loaded libqlin (ctypes).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        p = path or os.environ.get("QLIN_LIBRARY", LIB_PATH)
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libqlin.so not found at {p}; build it with "
+                "`python -m int8_qmv_qmm_gb300.build_lib` (needs nvcc)")
+        handle = ctypes.CDLL(p)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype, fn.argtypes = res, args
+        _LIB = handle
+    return _LIB
+
+
+def _check(status: int):
+    if status != 0:
+        L = lib()
+        raise QlinError(status, f"{L.qlin_status_str(status).decode()}: "
+                                f"{L.qlin_last_error().decode()}")
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(t.data_ptr() if t is not None and t.numel() else 0)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def quantize_affine(w: torch.Tensor, bits: int, group_size: int = GROUP_SIZE,
+                    sdtype: torch.dtype = torch.float16):
+    """Quantise float32 W[N, K] on the GPU -> (wq, scales, biases)."""
+    _need_cuda(w)
+    if w.dtype != torch.float32 or w.dim() != 2:
+        raise ValueError("w must be a 2-D float32 tensor")
+    n, k = w.shape
+    wq = torch.empty((n, k * bits // 32), dtype=torch.int32, device=w.device)
+    sc = torch.empty((n, k // group_size), dtype=sdtype, device=w.device)
+    bi = torch.empty_like(sc)
+    _check(lib().qlin_quantize_affine(_ptr(w), n, k, bits, group_size, _DTYPE_CODE[sdtype],
+                                      _ptr(wq), _ptr(sc), _ptr(bi), _stream(w)))
+    return wq, sc, bi
+
+
+def dequant(wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, bits: int,
+            group_size: int = GROUP_SIZE, out_dtype: torch.dtype | None = None) -> torch.Tensor:
+    """Materialise w_hat[N, K] = RNE(q*scale + bias) (unfused reference path)."""
+    _need_cuda(wq, scales, biases)
+    n = wq.shape[0]
+    k = wq.shape[1] * 32 // bits
+    out_dtype = out_dtype or scales.dtype
+    out = torch.empty((n, k), dtype=out_dtype, device=wq.device)
+    _check(lib().qlin_dequant(_ptr(wq), _ptr(scales), _ptr(biases), n, k, bits, group_size,
+                              _DTYPE_CODE[scales.dtype], _DTYPE_CODE[out_dtype], _ptr(out),
+                              _stream(wq)))
+    return out
+
+
+def _matmul(name: str, x, wq, scales, biases, bits, group_size, out):
+    _need_cuda(x, wq, scales, biases)
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    m, k = x.shape
+    n = wq.shape[0]
+    if wq.shape[1] * 32 // bits != k:
+        raise ValueError("wq does not match K")
+    if out is None:
+        out = torch.empty((m, n), dtype=x.dtype, device=x.device)
+    _need_cuda(out)
+    fn = getattr(lib(), name)
+    _check(fn(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(out), m, n, k, bits,
+              group_size, _DTYPE_CODE[x.dtype], _stream(x)))
+    return out
+
+
+def qmv(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
+    """y = x . w_hat^T on CUDA cores (decode, small M)."""
+    return _matmul("qlin_qmv", x, wq, scales, biases, bits, group_size, out)
+
+
+def qmm(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
+    """y = x . w_hat^T on the tcgen05 tensor cores (batched decode, prefill)."""
+    return _matmul("qlin_qmm", x, wq, scales, biases, bits, group_size, out)
+
+
+def linear(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
+    """qmv below the measured crossover M, qmm above it."""
+    return _matmul("qlin_linear", x, wq, scales, biases, bits, group_size, out)
+
+
+def crossover_m(n: int, k: int, bits: int) -> int:
+    return int(lib().qlin_crossover_m(n, k, bits))
+
+
+def device_status() -> int:
+    """Reads and clears the kernels' device status word (synchronises)."""
+    v = ctypes.c_int(0)
+    _check(lib().qlin_device_status(ctypes.byref(v)))
+    return v.value

@@ -1,0 +1,203 @@
+// Public C entry points of libqlin: argument validation, then dispatch to the
+// launchers.  Nothing is launched unless every check passes.
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "qlin_internal.h"
+
+namespace qlin {
+
+static thread_local char g_last_error[512] = "";
+
+qlin_status fail(qlin_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+qlin_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(QLIN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return QLIN_OK;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qlin_status check_format(int64_t N, int64_t K, int bits, int group_size) {
+  if (bits != 4 && bits != 8) return fail(QLIN_ERR_UNSUPPORTED, "bits=%d (supported: 4, 8)", bits);
+  if (group_size != kGroup)
+    return fail(QLIN_ERR_UNSUPPORTED, "group_size=%d (supported: 64)", group_size);
+  if (N < 0) return fail(QLIN_ERR_INVALID_ARG, "N=%lld < 0", (long long)N);
+  if (K <= 0 || K % group_size)
+    return fail(QLIN_ERR_INVALID_ARG, "K=%lld must be a positive multiple of group_size=%d",
+                (long long)K, group_size);
+  if (N > (int64_t(1) << 31) || K > (int64_t(1) << 24))
+    return fail(QLIN_ERR_UNSUPPORTED, "N=%lld or K=%lld beyond the supported range",
+                (long long)N, (long long)K);
+  return QLIN_OK;
+}
+
+qlin_status check_act_dtype(qlin_dtype d, const char* what) {
+  if (d != QLIN_F16 && d != QLIN_BF16)
+    return fail(QLIN_ERR_UNSUPPORTED, "%s dtype %d (supported: QLIN_F16, QLIN_BF16)", what, (int)d);
+  return QLIN_OK;
+}
+
+using MatmulLauncher = qlin_status (*)(const void*, const uint32_t*, const void*, const void*,
+                                       void*, int64_t, int64_t, int64_t, int, qlin_dtype,
+                                       cudaStream_t);
+
+qlin_status matmul_entry(const char* name, MatmulLauncher launch, const void* x,
+                         const uint32_t* wq, const void* scales, const void* biases, void* y,
+                         int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                         qlin_dtype dtype, void* stream) {
+  qlin_status s = check_format(N, K, bits, group_size);
+  if (s != QLIN_OK) return s;
+  if ((s = check_act_dtype(dtype, "activation/scale")) != QLIN_OK) return s;
+  if (M < 0) return fail(QLIN_ERR_INVALID_ARG, "%s: M=%lld < 0", name, (long long)M);
+  if (M > (int64_t(1) << 31)) return fail(QLIN_ERR_UNSUPPORTED, "%s: M too large", name);
+  if (M == 0 || N == 0) return QLIN_OK;  // empty product: nothing to write
+  if (!x || !wq || !scales || !biases || !y)
+    return fail(QLIN_ERR_INVALID_ARG, "%s: null pointer argument", name);
+  if (!aligned(x, 16) || !aligned(wq, 16))
+    return fail(QLIN_ERR_MISALIGNED, "%s: x and wq must be 16-byte aligned", name);
+  if (!aligned(scales, 2) || !aligned(biases, 2) || !aligned(y, 2))
+    return fail(QLIN_ERR_MISALIGNED, "%s: scales, biases and y must be 2-byte aligned", name);
+  return launch(x, wq, scales, biases, y, M, N, K, bits, dtype,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace qlin
+
+using namespace qlin;
+
+extern "C" {
+
+const char* qlin_status_str(qlin_status s) {
+  switch (s) {
+    case QLIN_OK: return "QLIN_OK";
+    case QLIN_ERR_INVALID_ARG: return "QLIN_ERR_INVALID_ARG";
+    case QLIN_ERR_UNSUPPORTED: return "QLIN_ERR_UNSUPPORTED";
+    case QLIN_ERR_MISALIGNED: return "QLIN_ERR_MISALIGNED";
+    case QLIN_ERR_CUDA: return "QLIN_ERR_CUDA";
+    case QLIN_ERR_DEVICE_TIMEOUT: return "QLIN_ERR_DEVICE_TIMEOUT";
+  }
+  return "QLIN_ERR_UNKNOWN";
+}
+
+const char* qlin_last_error(void) { return g_last_error; }
+
+int qlin_version(void) { return 100; }
+
+qlin_status qlin_quantize_affine(const float* w, int64_t N, int64_t K, int bits, int group_size,
+                                 qlin_dtype sdtype, uint32_t* wq, void* scales, void* biases,
+                                 void* stream) {
+  g_last_error[0] = 0;
+  qlin_status s = check_format(N, K, bits, group_size);
+  if (s != QLIN_OK) return s;
+  if ((s = check_act_dtype(sdtype, "scale")) != QLIN_OK) return s;
+  if (N == 0) return QLIN_OK;
+  if (!w || !wq || !scales || !biases)
+    return fail(QLIN_ERR_INVALID_ARG, "qlin_quantize_affine: null pointer argument");
+  if (!aligned(w, 16) || !aligned(wq, 16))
+    return fail(QLIN_ERR_MISALIGNED, "qlin_quantize_affine: w and wq must be 16-byte aligned");
+  if (!aligned(scales, 2) || !aligned(biases, 2))
+    return fail(QLIN_ERR_MISALIGNED, "qlin_quantize_affine: scales/biases must be 2-byte aligned");
+  return launch_quantize(w, N, K, bits, sdtype, wq, scales, biases,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status qlin_dequant(const uint32_t* wq, const void* scales, const void* biases, int64_t N,
+                         int64_t K, int bits, int group_size, qlin_dtype sdtype,
+                         qlin_dtype out_dtype, void* w_out, void* stream) {
+  g_last_error[0] = 0;
+  qlin_status s = check_format(N, K, bits, group_size);
+  if (s != QLIN_OK) return s;
+  if ((s = check_act_dtype(sdtype, "scale")) != QLIN_OK) return s;
+  if (out_dtype != QLIN_F32 && out_dtype != sdtype)
+    return fail(QLIN_ERR_UNSUPPORTED,
+                "qlin_dequant: out_dtype must be QLIN_F32 or the scale dtype (%d)", (int)sdtype);
+  if (N == 0) return QLIN_OK;
+  if (!wq || !scales || !biases || !w_out)
+    return fail(QLIN_ERR_INVALID_ARG, "qlin_dequant: null pointer argument");
+  if (!aligned(wq, 16) || !aligned(w_out, 16))
+    return fail(QLIN_ERR_MISALIGNED, "qlin_dequant: wq and w_out must be 16-byte aligned");
+  if (!aligned(scales, 2) || !aligned(biases, 2))
+    return fail(QLIN_ERR_MISALIGNED, "qlin_dequant: scales/biases must be 2-byte aligned");
+  return launch_dequant(wq, scales, biases, N, K, bits, sdtype, out_dtype, w_out,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+qlin_status qlin_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                     void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                     qlin_dtype dtype, void* stream) {
+  g_last_error[0] = 0;
+  return matmul_entry("qlin_qmv", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
+                      group_size, dtype, stream);
+}
+
+qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                     void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                     qlin_dtype dtype, void* stream) {
+  g_last_error[0] = 0;
+  return matmul_entry("qlin_qmm", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,
+                      group_size, dtype, stream);
+}
+
+int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
+  (void)N;
+  (void)K;
+  (void)bits;
+  const char* env = getenv("QLIN_CROSSOVER_M");
+  if (env && *env) {
+    long long v = atoll(env);
+    if (v >= 1) return v;
+  }
+  return 2;
+}
+
+qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
+                        const void* biases, void* y, int64_t M, int64_t N, int64_t K, int bits,
+                        int group_size, qlin_dtype dtype, void* stream) {
+  g_last_error[0] = 0;
+  if (M < qlin_crossover_m(N, K, bits))
+    return matmul_entry("qlin_linear", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
+                        group_size, dtype, stream);
+  return matmul_entry("qlin_linear", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,
+                      group_size, dtype, stream);
+}
+
+qlin_status qlin_device_status(int* flags) {
+  g_last_error[0] = 0;
+  if (!flags) return fail(QLIN_ERR_INVALID_ARG, "qlin_device_status: null pointer");
+  unsigned f = 0;
+  cudaError_t e = qmm_take_device_status(&f);
+  if (e != cudaSuccess)
+    return fail(QLIN_ERR_CUDA, "qlin_device_status: %s", cudaGetErrorString(e));
+  *flags = static_cast<int>(f);
+  return QLIN_OK;
+}
+
+}  // extern "C"

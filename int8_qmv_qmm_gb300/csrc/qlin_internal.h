@@ -1,0 +1,38 @@
+// Internal declarations shared by the libqlin translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qlin.h"
+
+namespace qlin {
+
+// Records a formatted detail message for qlin_last_error() and returns s.
+qlin_status fail(qlin_status s, const char* fmt, ...);
+
+// Maps a CUDA runtime error (if any) from the last launch to a status.
+qlin_status check_launch(const char* what);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Launchers.  Arguments are already validated by the public entry points.
+qlin_status launch_quantize(const float* w, int64_t N, int64_t K, int bits, qlin_dtype sdtype,
+                            uint32_t* wq, void* scales, void* biases, cudaStream_t st);
+qlin_status launch_dequant(const uint32_t* wq, const void* scales, const void* biases, int64_t N,
+                           int64_t K, int bits, qlin_dtype sdtype, qlin_dtype out_dtype,
+                           void* w_out, cudaStream_t st);
+qlin_status launch_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                       void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
+                       cudaStream_t st);
+qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                       void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
+                       cudaStream_t st);
+
+// Reads and clears the qmm kernels' device status word.
+cudaError_t qmm_take_device_status(unsigned* flags);
+
+constexpr int kGroup = 64;
+
+}  // namespace qlin

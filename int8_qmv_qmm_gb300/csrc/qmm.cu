@@ -1,0 +1,491 @@
+// qmm: fused dequantise-into-matmul on the tcgen05 tensor cores (batched
+// decode and prefill).
+//
+// y[m][n] = sum_k x[m][k] * w_hat[n][k],  w_hat = q*scale + bias (per group of 64)
+//
+// The reconstructed weight only ever exists as a shared-memory operand tile:
+// it is never written to DRAM ("track(upstream-iree): fused dequant->matmul
+// for the packed int8 bandwidth win", section "The blocker (measured)").
+//
+// Orientation ("swap AB"): the MMA's M dimension is 128 weight rows and its N
+// dimension is a tile of BN tokens, so small batches (BN = 16..64) still use
+// the full 128-row MMA and large ones use BN = 128/256.
+//   D[n][m] (TMEM, f32) += W_hat[n][k] (smem, A operand) * x[m][k] (smem, B)
+//
+// Per CTA (one 128 x BN output tile, K loop in stages of one group = 64 k):
+//   warp 0      TMA producer: x tile [BN x 64] (128-byte swizzle) and the
+//               packed tile [128 rows x 64 codes] into stage s.
+//   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of K=16
+//               per stage, then tcgen05.commit to free the stage.
+//   warps 2..5  dequantisers (thread = weight row): unpack the row's 64 codes,
+//               w_hat = q*scale + bias in the operand type with one fused
+//               multiply-add (bit-identical to qlin_dequant's output), and
+//               store the 128-byte row into the A tile in the 128-byte swizzle
+//               layout the MMA descriptor expects.  After the K loop the same
+//               warps are the epilogue: tcgen05.ld of their TMEM lane quarter,
+//               RNE to the output type, coalesced stores along n.
+//
+// Every mbarrier wait is bounded (about 2 s); a wait that gives up records a
+// bit in a device status word, the CTA unwinds (waiting, bounded, for its own
+// TMA copies and MMAs in flight), frees its TMEM and exits.
+
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "device_common.cuh"
+#include "qlin_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace qlin {
+
+__device__ unsigned int g_qmm_status = 0;
+
+namespace {
+
+constexpr int kBM = 128;          // weight rows per tile (MMA M)
+constexpr int kBK = 64;           // k per stage (one group)
+constexpr int kThreads = 192;     // 6 warps
+
+enum : unsigned {
+  kStatusProducer = 1u,
+  kStatusMma = 2u,
+  kStatusDequant = 4u,
+  kStatusEpilogue = 8u,
+  kStatusTeardown = 16u,
+};
+
+__device__ __forceinline__ void report(unsigned bit) { atomicOr(&g_qmm_status, bit); }
+
+template <int BITS>
+struct Geo {
+  static constexpr int kWordsPerGroup = kBK * BITS / 32;           // 8 or 16
+  static constexpr int kPackedRowBytes = kWordsPerGroup * 4;       // 32 or 64
+  static constexpr int kPackedBytes = kBM * kPackedRowBytes;       // 4 or 8 KB
+};
+
+__host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
+
+template <int BITS, int BN>
+struct Layout {
+  static constexpr int kXBytes = BN * kBK * 2;           // x tile, 128-byte rows
+  static constexpr int kABytes = kBM * kBK * 2;          // dequantised tile
+  static constexpr int kWBytes = Geo<BITS>::kPackedBytes;
+  static constexpr int kStageBytes = round_up(kXBytes, 1024) + kABytes + round_up(kWBytes, 1024);
+  static constexpr int kTxBytes = kXBytes + kWBytes;
+  static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+};
+
+// ---- unpack + dequantise one 16-bit pair: returns (w_hat[2j], w_hat[2j+1])
+template <typename AT>
+__device__ __forceinline__ uint32_t fma_pair(uint32_t magic_pair, uint32_t s2, uint32_t b2) {
+  using T2 = typename Act<AT>::T2;
+  const uint32_t mq = Act<AT>::kMagic2;
+  T2 v = *reinterpret_cast<const T2*>(&magic_pair);
+  const T2 m = *reinterpret_cast<const T2*>(&mq);
+  const T2 q = __hsub2(v, m);  // exact: both are small integers plus the magic
+  const T2 r = __hfma2(q, *reinterpret_cast<const T2*>(&s2), *reinterpret_cast<const T2*>(&b2));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// 8 consecutive codes of a 4-bit word -> 8 reconstructed 16-bit weights.
+template <typename AT>
+__device__ __forceinline__ uint4 dequant_word4(uint32_t w, uint32_t s2, uint32_t b2) {
+  const uint32_t sh = w >> 4;
+  uint32_t out[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    // low half <- byte j of w (code 2j in bits 0..3), high half <- byte j of
+    // w >> 4 (code 2j+1 in bits 16..19)
+    const uint32_t sel = uint32_t(j) | (uint32_t(j) << 4) | (uint32_t(4 + j) << 8) |
+                         (uint32_t(4 + j) << 12);
+    const uint32_t t = __byte_perm(w, sh, sel);
+    out[j] = fma_pair<AT>((t & 0x000F000Fu) | Act<AT>::kMagic2, s2, b2);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// 4 codes of an 8-bit word -> 2 pairs.
+template <typename AT>
+__device__ __forceinline__ void dequant_word8(uint32_t w, uint32_t s2, uint32_t b2,
+                                              uint32_t& p0, uint32_t& p1);
+
+template <>
+__device__ __forceinline__ void dequant_word8<__half>(uint32_t w, uint32_t s2, uint32_t b2,
+                                                      uint32_t& p0, uint32_t& p1) {
+  // 0x64 in the high byte of each half: 1024 + code, exact for codes < 1024
+  p0 = fma_pair<__half>(__byte_perm(w, 0x64646464u, 0x4140u), s2, b2);
+  p1 = fma_pair<__half>(__byte_perm(w, 0x64646464u, 0x4342u), s2, b2);
+}
+
+template <>
+__device__ __forceinline__ void dequant_word8<__nv_bfloat16>(uint32_t w, uint32_t s2, uint32_t b2,
+                                                             uint32_t& p0, uint32_t& p1) {
+  // bfloat16 has 8 significant bits, too few for 128 + code; go through f32:
+  // 2^23 + code is exact, the subtraction is exact, and the code (< 256) is
+  // exact in bfloat16.
+  float f[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    f[i] = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | uint32_t(i))) - 8388608.0f;
+  const __nv_bfloat162 q01 = __floats2bfloat162_rn(f[0], f[1]);
+  const __nv_bfloat162 q23 = __floats2bfloat162_rn(f[2], f[3]);
+  const __nv_bfloat162 s = *reinterpret_cast<const __nv_bfloat162*>(&s2);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&b2);
+  const __nv_bfloat162 r0 = __hfma2(q01, s, b), r1 = __hfma2(q23, s, b);
+  p0 = *reinterpret_cast<const uint32_t*>(&r0);
+  p1 = *reinterpret_cast<const uint32_t*>(&r1);
+}
+
+template <typename AT>
+__device__ __forceinline__ uint32_t splat(AT v) {
+  const uint16_t u = *reinterpret_cast<const uint16_t*>(&v);
+  return uint32_t(u) | (uint32_t(u) << 16);
+}
+
+template <int BITS, typename AT, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+               const AT* __restrict__ scales, const AT* __restrict__ biases, AT* __restrict__ y,
+               int M, int N, int K, int stages) {
+  using L = Layout<BITS, BN>;
+  using G = Geo<BITS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw_base);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBM, m0 = blockIdx.y * BN;
+  const int kb_count = K / kBK;
+
+  // stage s: [x tile][A tile][packed tile]
+  auto x_addr = [&](int s) { return base + uint32_t(s * L::kStageBytes); };
+  auto a_addr = [&](int s) { return x_addr(s) + uint32_t(round_up(L::kXBytes, 1024)); };
+  auto w_addr = [&](int s) { return a_addr(s) + uint32_t(L::kABytes); };
+  const uint32_t bar_base = base + uint32_t(stages * L::kStageBytes);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (stages + s); };
+  auto afull_bar = [&](int s) { return bar_base + 8u * (2 * stages + s); };
+  const uint32_t acc_bar = bar_base + 8u * (3 * stages);
+  const uint32_t done_bar = acc_bar + 8u;
+  const uint32_t tmem_slot = done_bar + 8u;
+  uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(gbase + (tmem_slot - base));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1 + 4);  // MMA commit + one per dequant warp
+      ptx::mbar_init(afull_bar(s), 4);      // one per dequant warp
+    }
+    ptx::mbar_init(acc_bar, 1);
+    ptx::mbar_init(done_bar, 1);
+    ptx::fence_mbar_init();
+    ptx::tma_prefetch_desc(&tm_x);
+    ptx::tma_prefetch_desc(&tm_w);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, L::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot_ptr;
+
+  bool ok = true;
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < kb_count; ++kb) {
+        const int s = kb % stages;
+        const uint32_t round = uint32_t(kb / stages);
+        if (kb >= stages && !ptx::mbar_wait(empty_bar(s), (round - 1) & 1u)) {
+          report(kStatusProducer);
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(full_bar(s), L::kTxBytes);
+        ptx::tma_load_2d(x_addr(s), &tm_x, full_bar(s), kb * kBK, m0);
+        ptx::tma_load_2d(w_addr(s), &tm_w, full_bar(s), kb * G::kWordsPerGroup, n0);
+        ++issued;
+      }
+      if (!ok) {
+        // let the copies this CTA issued land before its shared memory goes away
+        const int first = issued > stages ? issued - stages : 0;
+        for (int kb = first; kb < issued; ++kb)
+          if (!ptx::mbar_wait(full_bar(kb % stages), uint32_t(kb / stages) & 1u))
+            report(kStatusTeardown);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t fmt = std::is_same<AT, __half>::value ? 0u : 1u;
+      constexpr uint32_t idesc = ptx::idesc_f16(fmt, kBM, BN);
+      bool any = false;
+      for (int kb = 0; kb < kb_count; ++kb) {
+        const int s = kb % stages;
+        const uint32_t par = uint32_t(kb / stages) & 1u;
+        if (!ptx::mbar_wait(afull_bar(s), par) || !ptx::mbar_wait(full_bar(s), par)) {
+          report(kStatusMma);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint64_t ad = ptx::sw128_kmajor_desc(a_addr(s));
+        const uint64_t bd = ptx::sw128_kmajor_desc(x_addr(s));
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // +32 bytes along K = +2 in the descriptor's 16-byte address units
+          ptx::mma_f16_ss(tmem_base, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
+                          (kb > 0 || kk > 0) ? 1u : 0u);
+        }
+        any = true;
+        ptx::mma_commit(empty_bar(s));
+      }
+      ptx::mma_commit(ok ? acc_bar : done_bar);
+      if (!ok && any && !ptx::mbar_wait(done_bar, 0)) report(kStatusTeardown);
+    }
+  } else {
+    // ------------------------------------------------ dequantise + epilogue
+    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;     // weight row within the tile
+    const int n = n0 + r;
+    const int gpr = K / kGroup;
+    const AT* srow = scales + int64_t(min(n, N - 1)) * gpr;
+    const AT* brow = biases + int64_t(min(n, N - 1)) * gpr;
+    const bool row_ok = n < N;
+    // scales/biases of the row, fetched 4 groups ahead of use
+    AT s_nxt[4], b_nxt[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      s_nxt[j] = j < gpr ? srow[j] : srow[0];
+      b_nxt[j] = j < gpr ? brow[j] : brow[0];
+    }
+    const int swz_a = r & 7;
+    for (int kb0 = 0; kb0 < kb_count && ok; kb0 += 4) {
+      AT s_cur[4], b_cur[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        s_cur[j] = s_nxt[j];
+        b_cur[j] = b_nxt[j];
+        if (kb0 + 4 + j < gpr) {
+          s_nxt[j] = srow[kb0 + 4 + j];
+          b_nxt[j] = brow[kb0 + 4 + j];
+        }
+      }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int kb = kb0 + j;
+      if (kb >= kb_count) break;
+      const int s = kb % stages;
+      const uint32_t par = uint32_t(kb / stages) & 1u;
+      const AT sc = s_cur[j], bc = b_cur[j];
+      if (!ptx::mbar_wait(full_bar(s), par)) {
+        report(kStatusDequant);
+        ok = false;
+        break;
+      }
+      const uint32_t s2 = row_ok ? splat(sc) : 0u, b2 = row_ok ? splat(bc) : 0u;
+      const uint8_t* wrow = gbase + (w_addr(s) - base) + r * G::kPackedRowBytes;
+      uint8_t* arow = gbase + (a_addr(s) - base) + r * 128;
+      if constexpr (BITS == 4) {
+        // packed rows are 32 bytes in the 32-byte TMA swizzle: chunk c of row
+        // r sits at chunk c ^ ((r >> 2) & 1)
+        const int sw = (r >> 2) & 1;
+        const uint4 lo = *reinterpret_cast<const uint4*>(wrow + ((0 ^ sw) << 4));
+        const uint4 hi = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
+        const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(arow + ((c ^ swz_a) << 4)) =
+              dequant_word4<AT>(words[c], s2, b2);
+      } else {
+        // packed rows are 64 bytes in the 64-byte TMA swizzle: chunk c of row
+        // r sits at chunk c ^ ((r >> 1) & 3)
+        const int sw = (r >> 1) & 3;
+        uint32_t words[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ sw) << 4));
+          words[4 * c] = v.x;
+          words[4 * c + 1] = v.y;
+          words[4 * c + 2] = v.z;
+          words[4 * c + 3] = v.w;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 o;
+          dequant_word8<AT>(words[2 * c], s2, b2, o.x, o.y);
+          dequant_word8<AT>(words[2 * c + 1], s2, b2, o.z, o.w);
+          *reinterpret_cast<uint4*>(arow + ((c ^ swz_a) << 4)) = o;
+        }
+      }
+      ptx::fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(afull_bar(s));
+        ptx::mbar_arrive(empty_bar(s));
+      }
+    }
+    }
+    // epilogue
+    if (ok) {
+      if (!ptx::mbar_wait(acc_bar, 0)) {
+        report(kStatusEpilogue);
+        ok = false;
+      }
+    }
+    if (ok) {
+      ptx::tc_fence_after();
+      const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t v[16];
+        ptx::tmem_ld_32x32b_x16(t_lane + uint32_t(c0), v);
+        ptx::tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int m = m0 + c0 + j;
+            if (m < M) y[int64_t(m) * N + n] = Act<AT>::from_f32_rn(__uint_as_float(v[j]));
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, L::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------- host
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+qlin_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+                     uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                     CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(QLIN_ERR_CUDA, "qlin_qmm: cuTensorMapEncodeTiled unavailable");
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(QLIN_ERR_CUDA, "qlin_qmm: cuTensorMapEncodeTiled failed (%d)", int(r));
+  return QLIN_OK;
+}
+
+template <int BITS, typename AT, int BN>
+qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                      void* y, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+  using L = Layout<BITS, BN>;
+  constexpr int kMaxSmem = 227 * 1024;
+  const int stages = std::min(8, (kMaxSmem - 1024 - 256) / L::kStageBytes);
+  if (stages < 2) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: tile does not fit");
+  const size_t smem = size_t(stages) * L::kStageBytes + 1024 + 256;
+
+  CUtensorMap tm_x, tm_w;
+  const CUtensorMapDataType xdt = std::is_same<AT, __half>::value
+                                      ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  qlin_status s = make_map(&tm_x, xdt, x, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, BN,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+  if (s != QLIN_OK) return s;
+  const uint64_t wpr = uint64_t(K) * BITS / 32;
+  s = make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, wq, wpr, uint64_t(N), wpr * 4,
+               Geo<BITS>::kWordsPerGroup, kBM,
+               BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
+  if (s != QLIN_OK) return s;
+
+  auto kern = qmm_kernel<BITS, AT, BN>;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
+        cudaSuccess)
+      return check_launch("qlin_qmm: cudaFuncSetAttribute");
+    attr_dev = dev;
+  }
+  const dim3 grid(unsigned((N + kBM - 1) / kBM), unsigned((M + BN - 1) / BN));
+  if (grid.y > 65535u) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: M too large");
+  kern<<<grid, kThreads, smem, st>>>(tm_x, tm_w, static_cast<const AT*>(scales),
+                                     static_cast<const AT*>(biases), static_cast<AT*>(y), int(M),
+                                     int(N), int(K), stages);
+  return check_launch("qmm_kernel");
+}
+
+template <int BITS, typename AT>
+qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                     void* y, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+  // Token tile: the whole batch when it is small; otherwise the largest tile
+  // that still gives every SM a CTA.
+  int bn = 16;
+  while (bn < 256 && bn < M) bn <<= 1;
+  const int64_t sms = sm_count();
+  const int64_t n_tiles = (N + kBM - 1) / kBM;
+  while (bn > 64 && n_tiles * ((M + bn - 1) / bn) < sms) bn >>= 1;
+  switch (bn) {
+    case 16: return launch_bn<BITS, AT, 16>(x, wq, scales, biases, y, M, N, K, st);
+    case 32: return launch_bn<BITS, AT, 32>(x, wq, scales, biases, y, M, N, K, st);
+    case 64: return launch_bn<BITS, AT, 64>(x, wq, scales, biases, y, M, N, K, st);
+    case 128: return launch_bn<BITS, AT, 128>(x, wq, scales, biases, y, M, N, K, st);
+    default: return launch_bn<BITS, AT, 256>(x, wq, scales, biases, y, M, N, K, st);
+  }
+}
+
+}  // namespace
+
+qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                       void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
+                       cudaStream_t st) {
+  if (dtype == QLIN_F16)
+    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, st)
+                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, st);
+  return bits == 4 ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, st)
+                   : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, st);
+}
+
+cudaError_t qmm_take_device_status(unsigned* flags) {
+  unsigned v = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(&v, g_qmm_status, sizeof(v));
+  if (e != cudaSuccess) return e;
+  const unsigned zero = 0;
+  e = cudaMemcpyToSymbol(g_qmm_status, &zero, sizeof(zero));
+  *flags = v;
+  return e;
+}
+
+}  // namespace qlin

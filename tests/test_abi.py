@@ -1,0 +1,111 @@
+"""Host-side tests of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before launching anything (so these
+run without a GPU: no call here reaches a kernel launch)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import int8_qmv_qmm_gb300 as q
+from int8_qmv_qmm_gb300 import build_lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "qlin.h")
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return q.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qlin_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("qlin_quantize_affine", "qlin_dequant", "qlin_qmv", "qlin_qmm", "qlin_linear"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    assert L.qlin_status_str(0) == b"QLIN_OK"
+    assert L.qlin_status_str(3) == b"QLIN_ERR_MISALIGNED"
+    assert L.qlin_version() >= 100
+
+
+FAKE = 0x10000  # 16-byte aligned fake device address; never dereferenced here
+
+
+def _qmv(L, fn="qlin_qmv", x=FAKE, wq=FAKE, s=FAKE, b=FAKE, y=FAKE, M=1, N=300, K=512, bits=4,
+         g=64, dt=q.QLIN_F16):
+    return getattr(L, fn)(ctypes.c_void_p(x), ctypes.c_void_p(wq), ctypes.c_void_p(s),
+                          ctypes.c_void_p(b), ctypes.c_void_p(y), M, N, K, bits, g, dt, None)
+
+
+@pytest.mark.parametrize("fn", ["qlin_qmv", "qlin_qmm", "qlin_linear"])
+def test_matmul_argument_validation(L, fn):
+    assert _qmv(L, fn, bits=3) == UNSUPPORTED
+    assert _qmv(L, fn, bits=2) == UNSUPPORTED
+    assert _qmv(L, fn, g=32) == UNSUPPORTED
+    assert _qmv(L, fn, g=128) == UNSUPPORTED
+    assert _qmv(L, fn, dt=q.QLIN_F32) == UNSUPPORTED
+    assert _qmv(L, fn, K=100) == INVALID
+    assert _qmv(L, fn, K=0) == INVALID
+    assert _qmv(L, fn, K=-64) == INVALID
+    assert _qmv(L, fn, M=-1) == INVALID
+    assert _qmv(L, fn, N=-1) == INVALID
+    assert _qmv(L, fn, x=0) == INVALID
+    assert _qmv(L, fn, y=0) == INVALID
+    assert _qmv(L, fn, x=FAKE + 8) == MISALIGNED
+    assert _qmv(L, fn, wq=FAKE + 4) == MISALIGNED
+    assert _qmv(L, fn, y=FAKE + 1) == MISALIGNED
+    # empty products launch nothing and succeed, even with null pointers
+    assert _qmv(L, fn, M=0, x=0, y=0) == OK
+    assert _qmv(L, fn, N=0, wq=0, s=0, b=0, y=0) == OK
+
+
+def test_error_detail_is_recorded(L):
+    assert _qmv(L, bits=5) == UNSUPPORTED
+    assert b"bits=5" in L.qlin_last_error()
+
+
+def test_quantize_and_dequant_validation(L):
+    vp = ctypes.c_void_p
+    assert L.qlin_quantize_affine(vp(FAKE), 4, 128, 4, 64, q.QLIN_F32, vp(FAKE), vp(FAKE),
+                                  vp(FAKE), None) == UNSUPPORTED
+    assert L.qlin_quantize_affine(vp(FAKE), 4, 100, 4, 64, q.QLIN_F16, vp(FAKE), vp(FAKE),
+                                  vp(FAKE), None) == INVALID
+    assert L.qlin_quantize_affine(vp(FAKE + 4), 4, 128, 4, 64, q.QLIN_F16, vp(FAKE), vp(FAKE),
+                                  vp(FAKE), None) == MISALIGNED
+    assert L.qlin_quantize_affine(vp(0), 0, 128, 4, 64, q.QLIN_F16, vp(0), vp(0), vp(0),
+                                  None) == OK
+    # dequant: output dtype must be f32 or the scale dtype
+    assert L.qlin_dequant(vp(FAKE), vp(FAKE), vp(FAKE), 4, 128, 4, 64, q.QLIN_F16, q.QLIN_BF16,
+                          vp(FAKE), None) == UNSUPPORTED
+    assert L.qlin_dequant(vp(FAKE), vp(FAKE), vp(FAKE), 4, 128, 8, 64, q.QLIN_BF16, q.QLIN_F32,
+                          vp(FAKE + 8), None) == MISALIGNED
+    assert L.qlin_dequant(vp(0), vp(FAKE), vp(FAKE), 4, 128, 8, 64, q.QLIN_BF16, q.QLIN_F32,
+                          vp(FAKE), None) == INVALID
+
+
+def test_device_status_rejects_null(L):
+    assert L.qlin_device_status(None) == INVALID
+
+
+def test_crossover_env_override(L, monkeypatch):
+    base = L.qlin_crossover_m(8192, 2048, 4)
+    assert base >= 1
+    monkeypatch.setenv("QLIN_CROSSOVER_M", "7")
+    assert L.qlin_crossover_m(8192, 2048, 4) == 7

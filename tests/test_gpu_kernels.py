@@ -1,0 +1,158 @@
+"""GPU parity of every kernel against the CPU oracle on seeded inputs, through
+the C ABI (via the ctypes binding).  Sizes span several tiles and ragged tails;
+codes, scales, biases and reconstructed weights must be bit-exact, outputs
+within |y - y_ref| <= 2e-3 * sum_k |x_k w_nk| + 1e-5 per element."""
+
+import numpy as np
+import pytest
+import torch
+
+import int8_qmv_qmm_gb300 as q
+from int8_qmv_qmm_gb300 import synthetic as S
+from oracle import qlin_oracle as O
+from tests.gpu_helpers import (TORCH_DT, as_u16, as_u32, assert_within_tolerance,
+                               canaries_intact, case, guarded)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int8_qmv_qmm_gb300 import build_lib
+    build_lib.build()
+    q.lib()
+    return torch.device("cuda:0")
+
+
+def _upload(dev, w, bits, dt):
+    return q.quantize_affine(torch.from_numpy(w).to(dev), bits, sdtype=TORCH_DT[dt])
+
+
+# ------------------------------------------------------------ quantisation
+@pytest.mark.parametrize("bits,dt,n,k", [(4, "f16", 300, 512), (8, "f16", 77, 192),
+                                         (4, "bf16", 129, 2048), (8, "bf16", 64, 64),
+                                         (4, "f16", 1, 64), (8, "f16", 3, 8192)])
+def test_quantize_bit_exact(dev, bits, dt, n, k):
+    w = S.weights_f32(bits * 100 + n, n, k)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    codes, scale, bias = O.quantize_affine(w, bits, 64, dt)
+    assert np.array_equal(as_u32(wq), O.pack(codes, bits))
+    assert np.array_equal(as_u16(sc), O.encode_bits(scale, dt))
+    assert np.array_equal(as_u16(bi), O.encode_bits(bias, dt))
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("bits", [4, 8])
+def test_quantize_edge_groups(dev, bits, dt):
+    """Constant groups (scale 0), tiny ranges (subnormal f16 scale), exact ties,
+    huge and negative values."""
+    rng = np.random.default_rng(7)
+    w = (rng.standard_normal((16, 256)) * 0.02).astype(np.float32)
+    w[0, :64] = 0.375                                    # constant: scale 0
+    w[1, :64] = np.float32(1e-3) + np.arange(64, dtype=np.float32) * np.float32(1e-8)  # tiny
+    qmax = (1 << bits) - 1
+    t = np.tile(np.array([0, qmax, 0.5, 1.5, 2.5, qmax - 0.5], dtype=np.float64), 11)[:64]
+    w[2, :64] = (-0.0625 + t * 2.0 ** -9).astype(np.float32)  # exact ties
+    w[3, 64:128] = rng.standard_normal(64).astype(np.float32) * 100
+    w[4, 128:] = -np.abs(w[4, 128:]) - 3.0
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    codes, scale, bias = O.quantize_affine(w, bits, 64, dt)
+    assert np.array_equal(as_u32(wq), O.pack(codes, bits))
+    assert np.array_equal(as_u16(sc), O.encode_bits(scale, dt))
+    assert np.array_equal(as_u16(bi), O.encode_bits(bias, dt))
+
+
+# ------------------------------------------------------------ dequant
+@pytest.mark.parametrize("bits,dt", [(4, "f16"), (8, "f16"), (4, "bf16"), (8, "bf16")])
+@pytest.mark.parametrize("out", ["f32", "same"])
+def test_dequant_bit_exact(dev, bits, dt, out):
+    n, k = 131, 1024
+    w = S.weights_f32(31 + bits, n, k)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    codes, scale, bias = O.quantize_affine(w, bits, 64, dt)
+    fmt = dt if out == "same" else "f32"
+    got = q.dequant(wq, sc, bi, bits, out_dtype=torch.float32 if out == "f32" else TORCH_DT[dt])
+    ref_bits = O.encode_bits(O.dequant(codes, scale, bias, 64, fmt), fmt)
+    got_bits = as_u32(got) if fmt == "f32" else as_u16(got)
+    assert np.array_equal(got_bits, ref_bits)
+
+
+# ------------------------------------------------------------ qmv
+QMV_CASES = [
+    (1, 300, 512, 4, "f16"), (1, 301, 512, 8, "f16"), (1, 1, 64, 4, "f16"),
+    (1, 3, 192, 8, "bf16"), (1, 2048, 2048, 4, "f16"), (1, 513, 8192, 8, "f16"),
+    (1, 700, 2048, 4, "bf16"), (2, 300, 512, 4, "f16"), (3, 301, 1024, 8, "bf16"),
+    (4, 129, 2048, 4, "bf16"), (5, 77, 512, 8, "f16"), (8, 300, 256, 4, "f16"),
+    (13, 64, 512, 4, "bf16"), (2, 1000, 4096, 8, "bf16"),
+]
+
+
+@pytest.mark.parametrize("m,n,k,bits,dt", QMV_CASES)
+def test_qmv_parity(dev, m, n, k, bits, dt):
+    w, x, ref = case(1000 + m * 7 + n, m, n, k, bits, dt)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    buf, y = guarded((m, n), TORCH_DT[dt], dev)
+    q.qmv(x.to(dev), wq, sc, bi, bits, out=y)
+    torch.cuda.synchronize()
+    assert canaries_intact(buf)
+    assert_within_tolerance(y, ref, f"qmv m={m} n={n} k={k} b={bits} {dt}")
+
+
+# ------------------------------------------------------------ qmm
+QMM_CASES = [
+    (1, 300, 512, 4, "f16"), (3, 3, 64, 8, "f16"), (17, 130, 192, 4, "bf16"),
+    (33, 300, 512, 8, "f16"), (64, 256, 1024, 4, "f16"), (129, 301, 512, 4, "bf16"),
+    (300, 200, 256, 8, "bf16"), (600, 384, 512, 4, "f16"), (257, 1, 128, 8, "f16"),
+    (16, 128, 64, 4, "f16"), (512, 1024, 2048, 8, "f16"),
+]
+
+
+@pytest.mark.parametrize("m,n,k,bits,dt", QMM_CASES)
+def test_qmm_parity(dev, m, n, k, bits, dt):
+    w, x, ref = case(2000 + m * 7 + n, m, n, k, bits, dt, outlier_frac=0.01 if m >= 100 else 0)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    buf, y = guarded((m, n), TORCH_DT[dt], dev)
+    q.qmm(x.to(dev), wq, sc, bi, bits, out=y)
+    torch.cuda.synchronize()
+    assert canaries_intact(buf)
+    assert_within_tolerance(y, ref, f"qmm m={m} n={n} k={k} b={bits} {dt}")
+
+
+@pytest.mark.parametrize("fn", ["qmv", "qmm"])
+@pytest.mark.parametrize("bits,dt", [(4, "f16"), (8, "f16"), (4, "bf16"), (8, "bf16")])
+def test_one_hot_rows_reproduce_dequant_bit_exactly(dev, fn, bits, dt):
+    """With x = e_k the product is a single exact term, so each output equals
+    the reconstructed weight w_hat[n][k] in the output precision: the fused
+    in-kernel reconstruction is bit-identical to the materialised one."""
+    n, k = 260, 512
+    w = S.weights_f32(77, n, k)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    cols = np.array([0, 1, 7, 63, 64, 200, 255, 256, 511])
+    x = torch.zeros((cols.size, k), dtype=TORCH_DT[dt])
+    x[np.arange(cols.size), cols] = 1
+    y = getattr(q, fn)(x.to(dev), wq, sc, bi, bits)
+    w_hat = q.dequant(wq, sc, bi, bits)
+    assert torch.equal(y.cpu(), w_hat[:, cols].t().contiguous().cpu())
+
+
+def test_linear_dispatches_both_paths(dev):
+    n, k, bits, dt = 300, 512, 4, "f16"
+    for m in (1, 40):
+        w, x, ref = case(5 + m, m, n, k, bits, dt)
+        wq, sc, bi = _upload(dev, w, bits, dt)
+        y = q.linear(x.to(dev), wq, sc, bi, bits)
+        assert_within_tolerance(y, ref, f"linear m={m}")
+
+
+def test_empty_batch_is_a_no_op(dev):
+    wq = torch.zeros((8, 64), dtype=torch.int32, device=dev)
+    sc = torch.zeros((8, 8), dtype=torch.float16, device=dev)
+    x = torch.zeros((0, 512), dtype=torch.float16, device=dev)
+    assert q.qmv(x, wq, sc, sc, 4).shape == (0, 8)
+    assert q.qmm(x, wq, sc, sc, 4).shape == (0, 8)
+
+
+def test_no_kernel_gave_up_a_wait(dev):
+    assert q.device_status() == 0
