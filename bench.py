@@ -1,0 +1,557 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused packed-weight decode step (and the prefill qmm).
+
+One step = one Llama-3.2-1B-shaped decode step, M = 1, 8-bit codes, group 64,
+f16 activations/scales/biases: 16 layers x (q, k, v, o, gate, up, down) + the
+lm_head (N = 128256), each linear a fused dequantise-into-matvec launch whose
+input is the previous launch's output, captured in one CUDA graph.  1.31 GB of
+packed weights stream per step, ten times the L2, so no flush is needed
+between steps.  The headline value is tokens/s-equivalent = steps / second.
+
+Also measured in the same run (reported beside the headline):
+  * per-launch qmv durations (CUDA events around each launch on its stream)
+    -> achieved HBM GB/s against the measured copy bandwidth (roofline);
+  * the tensor-core qmm at M = 2048 on the prefill shapes (8192x2048,
+    2048x8192, 2048x2048; 4- and 8-bit; f16; 1% outlier rows), L2 flushed
+    between timed launches -> TFLOP/s against the dense bf16 peak;
+  * end to end: per step the input copied from pinned host memory, the graph
+    replayed, the logits read back to pinned host memory;
+  * the CPU oracle on a bounded row sample of the same step, one core.
+
+--impl reference times the CPU oracle alone, as the reference arm.
+Multi-GPU: replicas only (the decode step does not shard here); under torchrun
+every rank runs its own replica and rank 0 reports the aggregate.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "M=1 qmv achieved HBM GB/s (% of peak); qmm TFLOP/s at M=2048; tokens/s eq"
+UNIT = "tokens/s-eq"
+WORKLOAD = ("llama-3.2-1b-shaped decode step: 16 x (q 2048x2048, k 512x2048, v 512x2048, "
+            "o 2048x2048, gate 8192x2048, up 8192x2048, down 2048x8192) + lm_head "
+            "128256x2048; M=1; 8-bit codes, group 64; f16 activations/scales/biases; "
+            "inputs chained from the previous launch's output; one CUDA graph")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+ORACLE_SAMPLE_STRIDE = 4   # cpu_baseline: every 4th output row of every linear (~25%)
+REFERENCE_STRIDE = 256     # reference arm: every 256th row per step (~0.4%)
+
+
+# ------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        out = {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops") if k in d}
+        out["bf16_tflops_sustained"] = float(d.get("bf16_tflops_sustained",
+                                                   out.get("bf16_tflops", 0)))
+        if "hbm_gbs" in out and "bf16_tflops" in out:
+            out["source"] = "measured"
+            return out
+    except (OSError, ValueError, KeyError):
+        pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def profile_traffic(profile_name: str, source_file: str):
+    """DRAM bytes per launch recorded by an ncu capture under profiles/, or
+    None when absent or when the kernel source changed since the capture."""
+    prof = os.path.join(ROOT, "profiles", profile_name)
+    src = os.path.join(ROOT, "int8_qmv_qmm_gb300", "csrc", source_file)
+    try:
+        fields = {}
+        with open(prof) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith(("traffic_bytes_per_launch",
+                                                            "source_sha256")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        with open(src, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if fields.get("source_sha256") != sha:
+            return None
+        return float(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clock / throttle reasons through NVML (ctypes) in a thread;
+    falls back to an `nvidia-smi -lms` subprocess.  Reads settings only."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, pci_bus_id: str | None, index: int = 0):
+        self.samples, self.reasons_mask, self.max_mhz = [], 0, None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._handle = None
+        self._proc = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            ok = False
+            if pci_bus_id:
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(),
+                                                         ctypes.byref(h)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            self._nvml, self._handle = nv, h
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+        except OSError:
+            self._nvml = None
+
+    def _loop(self):
+        nv, h = self._nvml, self._handle
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if get_reasons(h, ctypes.byref(rs)) == 0:
+                self.reasons_mask |= rs.value
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,"
+                     "clocks_event_reasons.active", "--format=csv,noheader,nounits",
+                     "-lms", "50", "-i", "0"], stdout=subprocess.PIPE, text=True)
+            except OSError:
+                self._proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self._nvml is not None:
+            self._stop.set()
+            self._thread.join()
+        elif self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate()
+            for line in out.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append(int(parts[0]))
+                    self.max_mhz = int(parts[1])
+                    self.reasons_mask |= int(parts[2], 16)
+                except (ValueError, IndexError):
+                    pass
+
+    def summary(self):
+        reasons = [name for bit, name in self.REASONS.items()
+                   if self.reasons_mask & bit and name != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "reasons": reasons}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        rank = dist.get_rank()
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def max_over_ranks(dist, value: float, device):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---------------------------------------------------------- CPU oracle leg
+def oracle_sample_child(stride: int, steps: int) -> dict:
+    """Runs in a child process with one BLAS thread: times the oracle's
+    per-token work (unpack + exact dequant + f64 matmul) over every
+    `stride`-th output row of every linear of the decode step, `steps` times.
+    Weight generation and quantisation (load-time work) are not timed."""
+    import numpy as np
+
+    from int8_qmv_qmm_gb300 import synthetic as S
+    from oracle import qlin_oracle as O
+
+    shapes = [(n, k) for _ in range(S.LLAMA_1B_LAYERS) for (_, n, k) in S.LLAMA_1B_LINEARS]
+    shapes.append(S.LLAMA_1B_LM_HEAD[1:])
+    prepared = []
+    for idx, (n, k) in enumerate(shapes):
+        rows = np.arange(0, n, stride)
+        w = S.weights_f32(S.weight_seed(2, idx), n, k, rows=rows)
+        codes, scale, bias = O.quantize_affine(w, 8, 64, "f16")
+        words = O.pack(codes, 8)
+        x = S.activations(S.weight_seed(2, idx), 1, k, "f16").float().numpy()
+        prepared.append((words, scale, bias, x, k))
+    sampled = sum(p[0].shape[0] * p[4] for p in prepared)
+    total = sum(n * k for n, k in shapes)
+    times = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        for words, scale, bias, x, k in prepared:
+            codes = O.unpack(words, 8, k)
+            w_hat = O.dequant_exact(codes, scale, bias, 64)
+            O.matmul_ref(x, w_hat)
+        times.append(time.perf_counter() - t0)
+    return {"times": times, "fraction": sampled / total}
+
+
+def run_oracle(stride: int, steps: int) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+               MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child",
+                        str(stride), str(steps)], env=env, stdout=subprocess.PIPE,
+                       stderr=subprocess.PIPE, text=True, timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle child failed: {r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    frac, times = res["fraction"], res["times"]
+    return {"value": len(times) * frac / sum(times), "fraction": frac, "times": times,
+            "sample": (f"every {stride}th output row of all 113 linears of the decode step "
+                       f"({frac * 100:.2f}% of the weights): unpack + exact dequant + f64 "
+                       f"matmul, {sum(times) / len(times):.2f} s per pass, one BLAS thread")}
+
+
+def run_oracle_baseline(stride: int = ORACLE_SAMPLE_STRIDE) -> dict:
+    r = run_oracle(stride, 4)
+    return {"value": r["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": r["sample"]}
+
+
+# ------------------------------------------------------------- GPU legs
+def time_qmm(q, device, peaks, reps: int = 10, warm: int = 3):
+    """Tensor-core qmm at M = 2048 on the prefill shapes, L2 flushed between
+    timed launches."""
+    import torch
+
+    from int8_qmv_qmm_gb300 import synthetic as S
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    rows = []
+    for bits in (4, 8):
+        for (n, k) in ((8192, 2048), (2048, 8192), (2048, 2048)):
+            m = 2048
+            w = torch.from_numpy(S.weights_f32(S.weight_seed(4, n + k + bits), n, k)).to(device)
+            wq, sc, bi = q.quantize_affine(w, bits, sdtype=torch.float16)
+            del w
+            x = S.activations(4, m, k, "f16", outlier_frac=0.01).to(device)
+            y = torch.empty((m, n), dtype=torch.float16, device=device)
+            for _ in range(warm):
+                q.qmm(x, wq, sc, bi, bits, out=y)
+            times = []
+            for _ in range(reps):
+                flush.add_(1.0)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                q.qmm(x, wq, sc, bi, bits, out=y)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e-3)
+            t = statistics.median(times)
+            flops = 2.0 * m * n * k
+            rows.append({"m": m, "n": n, "k": k, "bits": bits, "us": t * 1e6,
+                         "tflops": flops / t / 1e12})
+    best = max(r["tflops"] for r in rows)
+    mean = statistics.mean(r["tflops"] for r in rows)
+    return {
+        "tflops_mean": mean, "tflops_best": best, "cases": rows,
+        "roofline": {"bound": "tensor", "achieved": mean, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": mean / peaks["bf16_tflops"],
+                     "traffic": None,
+                     "note": f"f16 MMA; peak = dense bf16 burst ({peaks['source']}), "
+                             "f16/bf16 nominal ratio 1"},
+    }
+
+
+def crossover_sweep(q, device, reps: int = 10, warm: int = 3):
+    """qmv vs qmm on the batched-decode sweep (M = 1..32, 4-bit, bf16), L2
+    flushed between timed launches; the crossover is the smallest M from which
+    qmm is faster on every shape."""
+    import torch
+
+    from int8_qmv_qmm_gb300 import synthetic as S
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    table = []
+    for (n, k) in ((8192, 2048), (2048, 8192)):
+        w = torch.from_numpy(S.weights_f32(S.weight_seed(3, n), n, k)).to(device)
+        wq, sc, bi = q.quantize_affine(w, 4, sdtype=torch.bfloat16)
+        del w
+        for m in (1, 2, 4, 8, 16, 32):
+            x = S.activations(3, m, k, "bf16").to(device)
+            y = torch.empty((m, n), dtype=torch.bfloat16, device=device)
+            row = {"n": n, "k": k, "m": m}
+            for name in ("qmv", "qmm"):
+                fn = getattr(q, name)
+                for _ in range(warm):
+                    fn(x, wq, sc, bi, 4, out=y)
+                ts = []
+                for _ in range(reps):
+                    flush.add_(1.0)
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn(x, wq, sc, bi, 4, out=y)
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3)
+                row[name + "_us"] = statistics.median(ts)
+            row["packed_gbs_qmv"] = (wq.numel() * 4 + 2 * sc.numel() * 2) / row["qmv_us"] / 1e3
+            table.append(row)
+    cross = None
+    for m in (1, 2, 4, 8, 16, 32):
+        if all(r["qmm_us"] <= r["qmv_us"] for r in table if r["m"] == m):
+            cross = m
+            break
+    return {"crossover_m": cross, "table": table}
+
+
+def per_launch_durations(step, device, reps: int = 3):
+    """Each qmv launch of the step bracketed by CUDA events on its stream."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    n = step.n_launches
+    sums = [0.0] * n
+    for _ in range(reps):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+
+        def hook(i, when):
+            ev[i][0 if when == "before" else 1].record(stream)
+
+        step.launch_all(per_launch_hook=hook)
+        torch.cuda.synchronize(device)
+        for i in range(n):
+            sums[i] += ev[i][0].elapsed_time(ev[i][1]) * 1e-3
+    return [s / reps for s in sums]
+
+
+def bench_ours(args):
+    import torch
+
+    import int8_qmv_qmm_gb300 as q
+    from int8_qmv_qmm_gb300 import build_lib
+    from int8_qmv_qmm_gb300.decode_step import DecodeStep
+
+    dist, rank, world, local = dist_setup(args.gpus)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0 or dist is None:
+        build_lib.build()
+    barrier(dist)
+    q.lib()
+    peaks = load_peaks()
+
+    step = DecodeStep(device, bits=8, dtype=torch.float16, seed=2)
+    x_host = torch.randn((1, 2048), generator=torch.Generator().manual_seed(0)).to(
+        torch.float16).pin_memory()
+    step.x0.copy_(x_host)
+    step.capture()
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        step.replay()
+    torch.cuda.synchronize(device)
+
+    props = torch.cuda.get_device_properties(device)
+    pci = None
+    if hasattr(props, "pci_bus_id"):
+        pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                    props.pci_device_id)
+    # ---- timed region: exactly `steps` graph replays
+    sampler = ClockSampler(pci)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with sampler:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+    barrier(dist)
+    t_local = e0.elapsed_time(e1) * 1e-3
+    t = max_over_ranks(dist, t_local, device)
+    per_step = t / args.steps
+    value = world * args.steps / t
+
+    # ---- per-launch durations of the dominant kernel (qmv)
+    durs = per_launch_durations(step, device)
+    alg = step.algorithmic_bytes()
+    achieved = sum(alg) / sum(durs) / 1e9
+    top = max(range(step.n_launches), key=lambda i: durs[i])
+
+    # ---- end to end through the public API with host buffers
+    logits_host = torch.empty((1, step.logits.shape[1]), dtype=torch.float16).pin_memory()
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step.x0.copy_(x_host, non_blocking=True)
+        step.replay()
+        logits_host.copy_(step.logits, non_blocking=True)
+        stream.synchronize()
+    t_e2e = max_over_ranks(dist, time.perf_counter() - t0, device)
+    e2e_value = world * args.steps / t_e2e
+
+    qmm_res = None if args.no_qmm else time_qmm(q, device, peaks)
+    cross = None if args.no_qmm else crossover_sweep(q, device)
+    status = q.device_status()
+
+    if rank != 0:
+        return
+    cpu = None if args.no_cpu_baseline else run_oracle_baseline()
+    clocks = sampler.summary()
+    bytes_step = step.packed_bytes()
+    traffic = profile_traffic("qmv_decode_step.txt", "qmv.cu")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "weights": "u8 codes, affine g64, f16 scale/bias",
+                   "activations": "f16", "accumulate": "f32",
+                   "packed_bytes_per_step": bytes_step,
+                   "l2": "inputs larger than L2 (packed weights per step = %.0f MB)"
+                         % (bytes_step / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "qmv_step_gbs": bytes_step / per_step / 1e9,
+        "qmv_step_frac_of_peak": bytes_step / per_step / 1e9 / peaks["hbm_gbs"],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "qmv_kernel (all 113 launches of a step, per-launch events)",
+                     "algorithmic_bytes_per_launch": sum(alg) / len(alg),
+                     "mean_launch_us": sum(durs) / len(durs) * 1e6,
+                     "peak_source": peaks["source"],
+                     "largest_launch": {"name": step.linears[top][0],
+                                        "us": durs[top] * 1e6,
+                                        "gbs": alg[top] / durs[top] / 1e9}},
+        "qmm": qmm_res,
+        "crossover": cross,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
+                "d2h_bytes_per_step": logits_host.numel() * 2},
+        "gpu_launches": args.steps * step.n_launches,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_reference(args):
+    """The reference arm: the CPU oracle as it stands, each step a bounded
+    sample (every REFERENCE_STRIDE-th output row) of the same decode step."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    r = run_oracle(REFERENCE_STRIDE, args.steps)
+    value = r["value"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": r["sample"],
+                         "value": value, "unit": UNIT},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def profile_case(which: str, launches: int = 3):
+    """A small fixed case for ncu: `launches` back-to-back launches of one
+    kernel on one workload shape (no timing, no oracle).
+      qmv: the lm_head of the decode step (M=1, 128256x2048, 8-bit, f16),
+           279 MB of packed weights (above the L2 size);
+      qmm: M=2048, N=8192, K=2048, 4-bit, f16 (the largest prefill case)."""
+    import torch
+
+    import int8_qmv_qmm_gb300 as q
+    from int8_qmv_qmm_gb300 import build_lib
+    from int8_qmv_qmm_gb300 import synthetic as S
+    build_lib.build()
+    dev = torch.device("cuda", 0)
+    if which == "qmv":
+        m, n, k, bits, fn = 1, 128256, 2048, 8, q.qmv
+    else:
+        m, n, k, bits, fn = 2048, 8192, 2048, 4, q.qmm
+    w = torch.from_numpy(S.weights_f32(7, n, k)).to(dev)
+    wq, sc, bi = q.quantize_affine(w, bits, sdtype=torch.float16)
+    del w
+    x = S.activations(7, m, k, "f16").to(dev)
+    y = torch.empty((m, n), dtype=torch.float16, device=dev)
+    for _ in range(launches):
+        fn(x, wq, sc, bi, bits, out=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": which, "m": m, "n": n, "k": k, "bits": bits,
+                      "launches": launches, "status": q.device_status()}))
+
+
+def main():
+    if len(sys.argv) >= 2 and sys.argv[1] == "--oracle-child":
+        print(json.dumps(oracle_sample_child(int(sys.argv[2]), int(sys.argv[3]))), flush=True)
+        return
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-qmm", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["qmv", "qmm"],
+                    help="run a small fixed case for ncu instead of the benchmark")
+    args = ap.parse_args()
+    if args.profile:
+        profile_case(args.profile)
+        return
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

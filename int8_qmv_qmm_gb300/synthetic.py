@@ -42,21 +42,36 @@ def weight_seed(base_seed: int, index: int) -> int:
     return base_seed * 1000 + index
 
 
-def weights_f32(seed: int, n_rows: int, k: int, rows=None) -> np.ndarray:
-    """W[N, K] float32 ~ N(0, 0.02); ``rows`` selects a subset (same values)."""
+def weights_f32(seed: int, n_rows: int, k: int, rows=None, threads: int = 8) -> np.ndarray:
+    """W[N, K] float32 ~ N(0, 0.02); ``rows`` selects a subset (same values).
+
+    Row blocks are independent streams, so they are drawn on a few threads
+    (numpy releases the GIL while filling); the values do not depend on it.
+    """
     if rows is None:
         rows = np.arange(n_rows)
     rows = np.asarray(rows, dtype=np.int64)
     if rows.size and (rows.min() < 0 or rows.max() >= n_rows):
         raise IndexError("row out of range")
     out = np.empty((rows.size, k), dtype=np.float32)
-    for blk in np.unique(rows // ROW_BLOCK):
+    blocks = np.unique(rows // ROW_BLOCK)
+
+    def fill(blk):
         r0 = int(blk) * ROW_BLOCK
         nb = min(ROW_BLOCK, n_rows - r0)
         rng = np.random.default_rng([seed, int(blk)])
-        block = rng.standard_normal((nb, k), dtype=np.float32) * np.float32(WEIGHT_STD)
+        block = rng.standard_normal((nb, k), dtype=np.float32)
+        block *= np.float32(WEIGHT_STD)
         sel = np.nonzero(rows // ROW_BLOCK == blk)[0]
         out[sel] = block[rows[sel] - r0]
+
+    if threads > 1 and blocks.size > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=min(threads, blocks.size)) as ex:
+            list(ex.map(fill, blocks))
+    else:
+        for blk in blocks:
+            fill(blk)
     return out
 
 
