@@ -45,7 +45,8 @@ UNIT = "tokens/s-eq"
 WORKLOAD = ("llama-3.2-1b-shaped decode step: 16 x (q 2048x2048, k 512x2048, v 512x2048, "
             "o 2048x2048, gate 8192x2048, up 8192x2048, down 2048x8192) + lm_head "
             "128256x2048; M=1; 8-bit codes, group 64; f16 activations/scales/biases; "
-            "inputs chained from the previous launch's output; one CUDA graph")
+            "q/k/v and gate/up stored fused (65 launches); inputs chained from the previous "
+            "launch's output; launches overlapped (programmatic dependent launch); one CUDA graph")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 ORACLE_SAMPLE_STRIDE = 4   # cpu_baseline: every 4th output row of every linear (~25%)
 REFERENCE_STRIDE = 256     # reference arm: every 256th row per step (~0.4%)
@@ -279,6 +280,7 @@ def time_qmm(q, device, peaks, reps: int = 10, warm: int = 3):
             times = []
             for _ in range(reps):
                 flush.add_(1.0)
+                torch.cuda._sleep(100000)  # the host enqueues the events and launch meanwhile
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -327,6 +329,7 @@ def crossover_sweep(q, device, reps: int = 10, warm: int = 3):
                 ts = []
                 for _ in range(reps):
                     flush.add_(1.0)
+                    torch.cuda._sleep(100000)  # the host enqueues the events and launch meanwhile
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
@@ -346,11 +349,18 @@ def crossover_sweep(q, device, reps: int = 10, warm: int = 3):
 
 
 def per_launch_durations(step, device, reps: int = 3):
-    """Each qmv launch of the step bracketed by CUDA events on its stream."""
+    """Each launch of the step bracketed by CUDA events on its stream.  A GPU
+    sleep is queued first so that the host enqueues every launch and event
+    before the GPU reaches them: the events then time the kernels back to back
+    (as in the graph), not the host's launch latency.  The launches here are
+    plain stream-ordered ones (no overlap), so each duration is the kernel's
+    own."""
     import torch
     stream = torch.cuda.current_stream(device)
     n = step.n_launches
     sums = [0.0] * n
+    saved = step.overlap
+    step.overlap = False
     for _ in range(reps):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n)]
@@ -358,11 +368,29 @@ def per_launch_durations(step, device, reps: int = 3):
         def hook(i, when):
             ev[i][0 if when == "before" else 1].record(stream)
 
+        torch.cuda._sleep(int(2e7))  # ~10 ms at 2 GHz, longer than enqueuing the step
         step.launch_all(per_launch_hook=hook)
         torch.cuda.synchronize(device)
         for i in range(n):
             sums[i] += ev[i][0].elapsed_time(ev[i][1]) * 1e-3
+    step.overlap = saved
     return [s / reps for s in sums]
+
+
+def per_shape_summary(step, durs, alg):
+    """Mean duration and GB/s of the launches of each fused shape."""
+    out = {}
+    for u, d, b in zip(step.units, durs, alg):
+        e = out.setdefault(u["name"], {"n": u["N"], "k": u["K"], "launches": 0, "us": 0.0,
+                                       "bytes": 0})
+        e["launches"] += 1
+        e["us"] += d * 1e6
+        e["bytes"] += b
+    for e in out.values():
+        e["gbs"] = e["bytes"] / (e["us"] * 1e-6) / 1e9
+        e["us"] /= e["launches"]
+        del e["bytes"]
+    return out
 
 
 def bench_ours(args):
@@ -458,11 +486,13 @@ def bench_ours(args):
         "qmv_step_frac_of_peak": bytes_step / per_step / 1e9 / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "qmv_kernel (all 113 launches of a step, per-launch events)",
+                     "kernel": "qmv_kernel (all %d launches of a step, per-launch events)"
+                               % step.n_launches,
                      "algorithmic_bytes_per_launch": sum(alg) / len(alg),
                      "mean_launch_us": sum(durs) / len(durs) * 1e6,
                      "peak_source": peaks["source"],
-                     "largest_launch": {"name": step.linears[top][0],
+                     "per_shape": per_shape_summary(step, durs, alg),
+                     "largest_launch": {"name": step.units[top]["name"],
                                         "us": durs[top] * 1e6,
                                         "gbs": alg[top] / durs[top] / 1e9}},
         "qmm": qmm_res,
@@ -512,10 +542,10 @@ def profile_case(which: str, launches: int = 3):
     from int8_qmv_qmm_gb300 import synthetic as S
     build_lib.build()
     dev = torch.device("cuda", 0)
-    if which == "qmv":
-        m, n, k, bits, fn = 1, 128256, 2048, 8, q.qmv
-    else:
-        m, n, k, bits, fn = 2048, 8192, 2048, 4, q.qmm
+    cases = {"qmv": (1, 128256, 2048, 8, q.qmv), "qmv_o": (1, 2048, 2048, 8, q.qmv),
+             "qmv_gate_up": (1, 16384, 2048, 8, q.qmv), "qmv_down": (1, 2048, 8192, 8, q.qmv),
+             "qmm": (2048, 8192, 2048, 4, q.qmm)}
+    m, n, k, bits, fn = cases[which]
     w = torch.from_numpy(S.weights_f32(7, n, k)).to(dev)
     wq, sc, bi = q.quantize_affine(w, bits, sdtype=torch.float16)
     del w
@@ -539,7 +569,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-qmm", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["qmv", "qmm"],
+    ap.add_argument("--profile", choices=["qmv", "qmv_o", "qmv_gate_up", "qmv_down", "qmm"],
                     help="run a small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:

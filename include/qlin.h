@@ -121,6 +121,25 @@ qlin_status qlin_qmv(const void* x, const uint32_t* wq, const void* scales, cons
                      qlin_dtype dtype, void* stream);
 
 /*
+ * Launch flags for the *_ex entry points.
+ *
+ * QLIN_OVERLAP_PREVIOUS: launch as a programmatic dependent launch.  The
+ *   kernel may start while the preceding kernel on the stream is still
+ *   running and begins streaming its weights, scales and biases at once; it
+ *   reads x and writes y only after that kernel has completed and its writes
+ *   are visible.  The caller guarantees that the preceding work on the stream
+ *   does not write wq, scales or biases (true for resident weights in a
+ *   decode loop).  Hides launch and ramp-up time between dependent launches.
+ */
+#define QLIN_OVERLAP_PREVIOUS 1u
+
+/* qlin_qmv with launch flags (0 = same as qlin_qmv).  Unknown flag bits
+ * return QLIN_ERR_INVALID_ARG. */
+qlin_status qlin_qmv_ex(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                        void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                        qlin_dtype dtype, unsigned flags, void* stream);
+
+/*
  * The same product on the tensor cores (batched decode and prefill): packed
  * tiles are staged into shared memory by TMA, dequantised there to dtype
  * (bit-identical to qlin_dequant's dtype output) and fed to tcgen05 MMA with
@@ -143,10 +162,11 @@ qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits);
 
 /*
- * Read and clear the device status word of the current device (synchronises
+ * Read and clear the device status words of the current device (synchronises
  * the device).  *flags receives 0 when no kernel gave up a bounded wait since
- * the last call, else a bit mask of the waits that gave up.  Returns QLIN_OK,
- * or QLIN_ERR_CUDA if the device could not be read.
+ * the last call, else a bit mask of the waits that gave up (bits 0-7: the
+ * tensor-core kernel, bits 8-15: the CUDA-core kernel).  Returns QLIN_OK, or
+ * QLIN_ERR_CUDA if the device could not be read.
  */
 qlin_status qlin_device_status(int* flags);
 

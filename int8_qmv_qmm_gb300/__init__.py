@@ -28,6 +28,7 @@ __all__ = [
 ]
 
 QLIN_F32, QLIN_F16, QLIN_BF16 = 0, 1, 2
+QLIN_OVERLAP_PREVIOUS = 1
 _DTYPE_CODE = {torch.float32: QLIN_F32, torch.float16: QLIN_F16, torch.bfloat16: QLIN_BF16}
 GROUP_SIZE = 64
 
@@ -43,6 +44,7 @@ _SIGNATURES = {
     "qlin_dequant": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int,
                               _c_vp, _c_vp]),
     "qlin_qmv": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
+    "qlin_qmv_ex": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [ctypes.c_uint, _c_vp]),
     "qlin_qmm": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_linear": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_crossover_m": (_c_i64, [_c_i64, _c_i64, _c_int]),
@@ -127,7 +129,7 @@ def dequant(wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, bits: 
     return out
 
 
-def _matmul(name: str, x, wq, scales, biases, bits, group_size, out):
+def _matmul(name: str, x, wq, scales, biases, bits, group_size, out, flags=None):
     _need_cuda(x, wq, scales, biases)
     if x.dim() != 2:
         raise ValueError("x must be 2-D [M, K]")
@@ -139,13 +141,21 @@ def _matmul(name: str, x, wq, scales, biases, bits, group_size, out):
         out = torch.empty((m, n), dtype=x.dtype, device=x.device)
     _need_cuda(out)
     fn = getattr(lib(), name)
+    extra = () if flags is None else (flags,)
     _check(fn(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(out), m, n, k, bits,
-              group_size, _DTYPE_CODE[x.dtype], _stream(x)))
+              group_size, _DTYPE_CODE[x.dtype], *extra, _stream(x)))
     return out
 
 
-def qmv(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
-    """y = x . w_hat^T on CUDA cores (decode, small M)."""
+def qmv(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None, overlap_previous=False):
+    """y = x . w_hat^T on CUDA cores (decode, small M).
+
+    overlap_previous=True launches with QLIN_OVERLAP_PREVIOUS (programmatic
+    dependent launch): only valid when the preceding work on the stream does
+    not write wq/scales/biases."""
+    if overlap_previous:
+        return _matmul("qlin_qmv_ex", x, wq, scales, biases, bits, group_size, out,
+                       flags=QLIN_OVERLAP_PREVIOUS)
     return _matmul("qlin_qmv", x, wq, scales, biases, bits, group_size, out)
 
 

@@ -66,14 +66,16 @@ qlin_status check_act_dtype(qlin_dtype d, const char* what) {
 
 using MatmulLauncher = qlin_status (*)(const void*, const uint32_t*, const void*, const void*,
                                        void*, int64_t, int64_t, int64_t, int, qlin_dtype,
-                                       cudaStream_t);
+                                       unsigned, cudaStream_t);
 
 qlin_status matmul_entry(const char* name, MatmulLauncher launch, const void* x,
                          const uint32_t* wq, const void* scales, const void* biases, void* y,
                          int64_t M, int64_t N, int64_t K, int bits, int group_size,
-                         qlin_dtype dtype, void* stream) {
+                         qlin_dtype dtype, unsigned flags, void* stream) {
   qlin_status s = check_format(N, K, bits, group_size);
   if (s != QLIN_OK) return s;
+  if (flags & ~unsigned(QLIN_OVERLAP_PREVIOUS))
+    return fail(QLIN_ERR_INVALID_ARG, "%s: unknown flags 0x%x", name, flags);
   if ((s = check_act_dtype(dtype, "activation/scale")) != QLIN_OK) return s;
   if (M < 0) return fail(QLIN_ERR_INVALID_ARG, "%s: M=%lld < 0", name, (long long)M);
   if (M > (int64_t(1) << 31)) return fail(QLIN_ERR_UNSUPPORTED, "%s: M too large", name);
@@ -84,7 +86,7 @@ qlin_status matmul_entry(const char* name, MatmulLauncher launch, const void* x,
     return fail(QLIN_ERR_MISALIGNED, "%s: x and wq must be 16-byte aligned", name);
   if (!aligned(scales, 2) || !aligned(biases, 2) || !aligned(y, 2))
     return fail(QLIN_ERR_MISALIGNED, "%s: scales, biases and y must be 2-byte aligned", name);
-  return launch(x, wq, scales, biases, y, M, N, K, bits, dtype,
+  return launch(x, wq, scales, biases, y, M, N, K, bits, dtype, flags,
                 reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -155,7 +157,15 @@ qlin_status qlin_qmv(const void* x, const uint32_t* wq, const void* scales, cons
                      qlin_dtype dtype, void* stream) {
   g_last_error[0] = 0;
   return matmul_entry("qlin_qmv", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
-                      group_size, dtype, stream);
+                      group_size, dtype, 0u, stream);
+}
+
+qlin_status qlin_qmv_ex(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                        void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                        qlin_dtype dtype, unsigned flags, void* stream) {
+  g_last_error[0] = 0;
+  return matmul_entry("qlin_qmv_ex", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
+                      group_size, dtype, flags, stream);
 }
 
 qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
@@ -163,7 +173,7 @@ qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, cons
                      qlin_dtype dtype, void* stream) {
   g_last_error[0] = 0;
   return matmul_entry("qlin_qmm", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,
-                      group_size, dtype, stream);
+                      group_size, dtype, 0u, stream);
 }
 
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
@@ -184,19 +194,22 @@ qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
   g_last_error[0] = 0;
   if (M < qlin_crossover_m(N, K, bits))
     return matmul_entry("qlin_linear", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
-                        group_size, dtype, stream);
+                        group_size, dtype, 0u, stream);
   return matmul_entry("qlin_linear", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,
-                      group_size, dtype, stream);
+                      group_size, dtype, 0u, stream);
 }
 
 qlin_status qlin_device_status(int* flags) {
   g_last_error[0] = 0;
   if (!flags) return fail(QLIN_ERR_INVALID_ARG, "qlin_device_status: null pointer");
-  unsigned f = 0;
-  cudaError_t e = qmm_take_device_status(&f);
+  unsigned fm = 0, fv = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = qmm_take_device_status(&fm);
+  if (e == cudaSuccess) e = qmv_take_device_status(&fv);
   if (e != cudaSuccess)
     return fail(QLIN_ERR_CUDA, "qlin_device_status: %s", cudaGetErrorString(e));
-  *flags = static_cast<int>(f);
+  // qmm waits in the low byte, qmv waits in the next one
+  *flags = static_cast<int>((fm & 0xffu) | ((fv & 0xffu) << 8));
   return QLIN_OK;
 }
 

@@ -44,9 +44,21 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return r;
 }
 
-template <typename T>
-__device__ __forceinline__ T ldg_nc(const T* p) {
-  return __ldg(p);
+// Asks L2 to fetch [p, p + bytes) (p and bytes multiples of 16); no data
+// comes back to the SM.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  if (bytes)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: wait until the preceding kernel on the stream
+// has completed and its writes are visible (returns at once when the launch
+// has no programmatic dependency), and allow the next kernel to launch early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace qlin

@@ -25,13 +25,14 @@ qlin_status launch_dequant(const uint32_t* wq, const void* scales, const void* b
                            void* w_out, cudaStream_t st);
 qlin_status launch_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       cudaStream_t st);
+                       unsigned flags, cudaStream_t st);
 qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       cudaStream_t st);
+                       unsigned flags, cudaStream_t st);
 
-// Reads and clears the qmm kernels' device status word.
+// Read and clear the kernels' device status words (no synchronisation).
 cudaError_t qmm_take_device_status(unsigned* flags);
+cudaError_t qmv_take_device_status(unsigned* flags);
 
 constexpr int kGroup = 64;
 

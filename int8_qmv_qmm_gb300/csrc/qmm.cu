@@ -468,7 +468,8 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
 
 qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       cudaStream_t st) {
+                       unsigned flags, cudaStream_t st) {
+  (void)flags;
   if (dtype == QLIN_F16)
     return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, st)
                      : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, st);
@@ -478,9 +479,7 @@ qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, co
 
 cudaError_t qmm_take_device_status(unsigned* flags) {
   unsigned v = 0;
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return e;
-  e = cudaMemcpyFromSymbol(&v, g_qmm_status, sizeof(v));
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_qmm_status, sizeof(v));
   if (e != cudaSuccess) return e;
   const unsigned zero = 0;
   e = cudaMemcpyToSymbol(g_qmm_status, &zero, sizeof(zero));

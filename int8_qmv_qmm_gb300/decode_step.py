@@ -1,22 +1,26 @@
 """A Llama-3.2-1B-shaped decode step made only of fused packed linears.
 
 Sixteen layers of the seven decoder linears (q, k, v, o, gate, up, down) plus
-the lm_head, M = 1, every weight distinct and resident packed in HBM.  The
+the lm_head, M = 1, every weight distinct and resident packed in HBM.  As in
+most inference engines, q/k/v and gate/up are stored as one fused matrix each
+(their rows concatenated; quantisation is per row and group, so this changes
+no bit of any row), which makes the step 4 launches per layer + 1 = 65.  The
 launches are chained the way a decoder's linears depend on each other, with
 the non-linear parts (attention, norms, activation) left out:
 
-    q, k, v   <- x_l                    (shared input)
-    o         <- y_q                    (stands in for the attention output)
-    gate, up  <- y_o                    (stands in for the normed residual)
-    down      <- y_gate                 (stands in for act(gate) * up)
-    x_{l+1}   =  y_down
-    logits    <- lm_head(x_16)
+    qkv      <- x_l
+    o        <- y_q          (stands in for the attention output)
+    gate_up  <- y_o          (stands in for the normed residual)
+    down     <- y_gate       (stands in for act(gate) * up)
+    x_{l+1}  =  y_down
+    logits   <- lm_head(x_16)
 
-so each launch reads what the previous one wrote: stream order serialises
-them exactly as a real decode step would.  The pages measure the packed decode
-step at ~678 dispatches ("epic: realize low-precision / quantized performance
-on the OpenXLA (IREE) backend", section "The measured fusion gate"); here it is
-113 launches of the fused kernel, captured once into a CUDA graph.
+so each launch reads what the previous one wrote.  Every launch after the
+first is a programmatic dependent launch: it starts streaming its (resident,
+never rewritten) weights while its predecessor finishes, and reads its input
+only after the predecessor completes.  The pages measure the packed decode step
+at ~678 dispatches ("epic: realize low-precision / quantized performance on the
+OpenXLA (IREE) backend", section "The measured fusion gate").
 """
 
 from __future__ import annotations
@@ -26,87 +30,99 @@ import torch
 from . import qmv, quantize_affine
 from . import synthetic as S
 
+_FUSED = (("qkv", ("q_proj", "k_proj", "v_proj")), ("o", ("o_proj",)),
+          ("gate_up", ("gate_proj", "up_proj")), ("down", ("down_proj",)))
+
 
 class DecodeStep:
     def __init__(self, device, bits: int = 8, dtype: torch.dtype = torch.float16,
                  seed: int = 2, layers: int = S.LLAMA_1B_LAYERS, lm_head: bool = True,
-                 progress=None):
+                 overlap: bool = True):
         self.device = torch.device(device)
         self.bits = bits
         self.dtype = dtype
-        self.linears = []  # (name, layer, N, K, wq, scales, biases, weight seed)
+        self.overlap = overlap
+        shapes = {name: (n, k) for name, n, k in S.LLAMA_1B_LINEARS}
+        # original linears, in the order of the weight seeds:
+        # (name, layer, N, K, unit index, first row in the unit, weight seed)
+        self.linears = []
+        self.units = []  # dicts: name, layer, N, K, wq, scales, biases, out
         idx = 0
         for layer in range(layers):
+            seeds = {}
             for name, n, k in S.LLAMA_1B_LINEARS:
-                self._add(name, layer, n, k, S.weight_seed(seed, idx))
+                seeds[name] = S.weight_seed(seed, idx)
                 idx += 1
-                if progress:
-                    progress(idx)
+            for uname, parts in _FUSED:
+                k = shapes[parts[0]][1]
+                rows, ws = 0, []
+                for p in parts:
+                    n = shapes[p][0]
+                    self.linears.append((p, layer, n, k, len(self.units), rows, seeds[p]))
+                    ws.append(torch.from_numpy(S.weights_f32(seeds[p], n, k)))
+                    rows += n
+                self._add_unit(uname, layer, torch.cat(ws).to(self.device))
         if lm_head:
             name, n, k = S.LLAMA_1B_LM_HEAD
-            self._add(name, layers, n, k, S.weight_seed(seed, idx))
+            wseed = S.weight_seed(seed, idx)
+            self.linears.append((name, layers, n, k, len(self.units), 0, wseed))
+            self._add_unit(name, layers, torch.from_numpy(S.weights_f32(wseed, n, k)).to(self.device))
         self.layers = layers
         hidden = S.LLAMA_1B_LINEARS[0][2]
         self.x0 = torch.zeros((1, hidden), dtype=dtype, device=self.device)
-        self.outputs = [torch.empty((1, n), dtype=dtype, device=self.device)
-                        for (_, _, n, _, _, _, _, _) in self.linears]
         self.graph = None
 
-    def _add(self, name, layer, n, k, wseed):
-        w = torch.from_numpy(S.weights_f32(wseed, n, k)).to(self.device)
+    def _add_unit(self, name, layer, w):
+        n, k = w.shape
         wq, sc, bi = quantize_affine(w, self.bits, sdtype=self.dtype)
         del w
-        self.linears.append((name, layer, n, k, wq, sc, bi, wseed))
+        out = torch.empty((1, n), dtype=self.dtype, device=self.device)
+        self.units.append(dict(name=name, layer=layer, N=n, K=k, wq=wq, scales=sc, biases=bi,
+                               out=out))
 
     # ------------------------------------------------------------------ sizes
     @property
     def n_launches(self) -> int:
-        return len(self.linears)
+        return len(self.units)
 
     def packed_bytes(self) -> int:
         """Bytes of codes + scales + biases streamed per step."""
-        tot = 0
-        for (_, _, n, k, wq, sc, bi, _) in self.linears:
-            tot += wq.numel() * 4 + sc.numel() * sc.element_size() + bi.numel() * bi.element_size()
-        return tot
+        return sum(u["wq"].numel() * 4 + (u["scales"].numel() + u["biases"].numel()) *
+                   u["scales"].element_size() for u in self.units)
 
     def algorithmic_bytes(self):
         """Per launch: packed weights + x read + y written."""
-        out = []
-        for (_, _, n, k, wq, sc, bi, _) in self.linears:
-            out.append(wq.numel() * 4 + (sc.numel() + bi.numel()) * sc.element_size()
-                       + (k + n) * self.x0.element_size())
-        return out
+        es = self.x0.element_size()
+        return [u["wq"].numel() * 4 + (u["scales"].numel() + u["biases"].numel()) *
+                u["scales"].element_size() + (u["K"] + u["N"]) * es for u in self.units]
 
     # ---------------------------------------------------------------- launches
-    def input_of(self, i: int) -> torch.Tensor:
-        """The tensor linear ``i`` reads in the chained step."""
-        name, layer = self.linears[i][0], self.linears[i][1]
-        base = 7 * layer
-        if name in ("q_proj", "k_proj", "v_proj"):
-            return self.x0 if layer == 0 else self.outputs[base - 1]
-        if name == "o_proj":
-            return self.outputs[base + 0]
-        if name in ("gate_proj", "up_proj"):
-            return self.outputs[base + 3]
-        if name == "down_proj":
-            return self.outputs[base + 4]
-        # lm_head
-        return self.outputs[base - 1] if self.layers else self.x0
+    def input_of(self, u: int) -> torch.Tensor:
+        """The tensor launch ``u`` reads in the chained step."""
+        name = self.units[u]["name"]
+        if name == "qkv":
+            return self.x0 if u == 0 else self.units[u - 1]["out"]
+        if name == "o":
+            return self.units[u - 1]["out"][:, :2048]            # q
+        if name == "gate_up":
+            return self.units[u - 1]["out"]
+        if name == "down":
+            return self.units[u - 1]["out"][:, :8192]            # gate
+        return self.units[u - 1]["out"] if u else self.x0      # lm_head
 
-    def run_linear(self, i: int, x: torch.Tensor, out: torch.Tensor | None = None):
-        """Linear ``i`` on an arbitrary input (same kernel and launch config)."""
-        _, _, n, k, wq, sc, bi, _ = self.linears[i]
-        return qmv(x, wq, sc, bi, self.bits, out=out)
+    def launch(self, u: int, x: torch.Tensor, out: torch.Tensor | None = None,
+               overlap: bool = False):
+        d = self.units[u]
+        return qmv(x, d["wq"], d["scales"], d["biases"], self.bits,
+                   out=d["out"] if out is None else out, overlap_previous=overlap)
 
     def launch_all(self, per_launch_hook=None):
-        for i in range(len(self.linears)):
-            _, _, n, k, wq, sc, bi, _ = self.linears[i]
+        for u in range(len(self.units)):
             if per_launch_hook:
-                per_launch_hook(i, "before")
-            qmv(self.input_of(i), wq, sc, bi, self.bits, out=self.outputs[i])
+                per_launch_hook(u, "before")
+            self.launch(u, self.input_of(u), overlap=self.overlap and u > 0)
             if per_launch_hook:
-                per_launch_hook(i, "after")
+                per_launch_hook(u, "after")
 
     def capture(self, stream: torch.cuda.Stream | None = None):
         """Capture one step into a CUDA graph (after one eager warm-up)."""
@@ -123,5 +139,19 @@ class DecodeStep:
 
     @property
     def logits(self) -> torch.Tensor:
-        return self.outputs[-1]
+        return self.units[-1]["out"]
 
+    # ----------------------------------------------- per original linear (tests)
+    def linear_rows(self, i: int):
+        """(name, layer, N, K, wq rows, scales rows, biases rows, weight seed)."""
+        name, layer, n, k, u, r0, wseed = self.linears[i]
+        d = self.units[u]
+        return (name, layer, n, k, d["wq"][r0:r0 + n], d["scales"][r0:r0 + n],
+                d["biases"][r0:r0 + n], wseed)
+
+    def run_linear(self, i: int, x: torch.Tensor):
+        """Linear ``i`` on an arbitrary input, through its unit's own launch."""
+        name, layer, n, k, u, r0, wseed = self.linears[i]
+        out = torch.empty((x.shape[0], self.units[u]["N"]), dtype=self.dtype, device=self.device)
+        self.launch(u, x, out=out)
+        return out[:, r0:r0 + n]

@@ -61,29 +61,37 @@ def test_prefill_qmm(dev, m, nk, bits):
 
 
 def test_full_decode_step_sampled_rows(dev):
-    """All 113 linears of the 8-bit decode step, each run on fresh synthetic
-    input through the step's own launch; 48 sampled rows per linear are
-    checked against the oracle (codes bit-exact, outputs within tolerance).
-    Then the chained graph replays and gives finite logits."""
+    """All 113 linears of the 8-bit decode step (stored fused as the step
+    launches them), each run on fresh synthetic input through its own launch;
+    48 sampled rows per linear are checked against the oracle (codes
+    bit-exact, outputs within tolerance).  Then the chained graph, with its
+    overlapped launches, replays and gives finite, repeatable logits."""
     from int8_qmv_qmm_gb300.decode_step import DecodeStep
     step = DecodeStep(dev, bits=8, dtype=torch.float16, seed=2)
+    assert len(step.linears) == 113 and step.n_launches == 65
     rng = np.random.default_rng(0)
-    for i, (name, layer, n, k, wq, sc, bi, wseed) in enumerate(step.linears):
+    for i in range(len(step.linears)):
+        name, layer, n, k, wq, sc, bi, wseed = step.linear_rows(i)
         rows = np.unique(np.concatenate([[0, n - 1], rng.choice(n, 46, replace=False)]))
         w_rows = S.weights_f32(wseed, n, k, rows=rows)
         x = S.activations(wseed, 1, k, "f16")
         r = O.linear_ref(x.float().numpy().astype(np.float64), w_rows, 8, 64, "f16")
         y = step.run_linear(i, x.to(dev))
-        assert np.array_equal(as_u32(wq[torch.from_numpy(rows).to(dev)]), r["words"]), name
-        assert_within_tolerance(y[:, torch.from_numpy(rows).to(dev)], r, f"{name} layer {layer}")
+        idx = torch.from_numpy(rows).to(dev)
+        assert np.array_equal(as_u32(wq[idx]), r["words"]), name
+        assert_within_tolerance(y[:, idx], r, f"{name} layer {layer}")
     step.x0.copy_(S.activations(9, 1, 2048, "f16").to(dev))
     step.capture()
     step.replay()
     torch.cuda.synchronize()
     assert torch.isfinite(step.logits.float()).all()
-    # replaying twice from the same input gives the same logits (no stale state)
     first = step.logits.clone()
     step.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(first, step.logits)
+    # the overlapped chain computes exactly what plain stream-ordered launches do
+    step.overlap = False
+    step.launch_all()
     torch.cuda.synchronize()
     assert torch.equal(first, step.logits)
     assert q.device_status() == 0
