@@ -3,14 +3,16 @@
 
 One step = one Llama-3.2-1B-shaped decode step, M = 1, 8-bit codes, group 64,
 f16 activations/scales/biases: 16 layers x (q, k, v, o, gate, up, down) + the
-lm_head (N = 128256), each linear a fused dequantise-into-matvec launch whose
-input is the previous launch's output, captured in one CUDA graph.  1.31 GB of
-packed weights stream per step, ten times the L2, so no flush is needed
-between steps.  The headline value is tokens/s-equivalent = steps / second.
+lm_head (N = 128256), each linear a fused dequantise-into-matvec whose input is
+an earlier linear's output: 65 launches (q/k/v and gate/up fused) overlapped
+with programmatic dependent launch, captured in one CUDA graph.  1.31 GB of packed weights stream
+per step, ten times the L2, so no flush is needed between steps.  The headline
+value is tokens/s-equivalent = steps / second.
 
 Also measured in the same run (reported beside the headline):
-  * per-launch qmv durations (CUDA events around each launch on its stream)
+  * each qmv launch's own duration (CUDA events around it on its stream)
     -> achieved HBM GB/s against the measured copy bandwidth (roofline);
+  * the same step as one persistent chain launch (qlin_qmv_chain);
   * the tensor-core qmm at M = 2048 on the prefill shapes (8192x2048,
     2048x8192, 2048x2048; 4- and 8-bit; f16; 1% outlier rows), L2 flushed
     between timed launches -> TFLOP/s against the dense bf16 peak;
@@ -45,8 +47,9 @@ UNIT = "tokens/s-eq"
 WORKLOAD = ("llama-3.2-1b-shaped decode step: 16 x (q 2048x2048, k 512x2048, v 512x2048, "
             "o 2048x2048, gate 8192x2048, up 8192x2048, down 2048x8192) + lm_head "
             "128256x2048; M=1; 8-bit codes, group 64; f16 activations/scales/biases; "
-            "q/k/v and gate/up stored fused (65 launches); inputs chained from the previous "
-            "launch's output; launches overlapped (programmatic dependent launch); one CUDA graph")
+            "q/k/v and gate/up stored fused (65 dependent launches); each launch's input is an "
+            "earlier launch's output; launches overlapped with programmatic dependent launch; "
+            "one CUDA graph")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 ORACLE_SAMPLE_STRIDE = 4   # cpu_baseline: every 4th output row of every linear (~25%)
 REFERENCE_STRIDE = 256     # reference arm: every 256th row per step (~0.4%)
@@ -393,6 +396,40 @@ def per_shape_summary(step, durs, alg):
     return out
 
 
+def time_eager(fn, device, reps: int = 5):
+    """Mean GPU duration of fn() (one or more launches on the current stream),
+    events recorded after a GPU sleep so that host enqueue time is excluded."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    tot = 0.0
+    for _ in range(reps):
+        torch.cuda._sleep(int(2e7))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1) * 1e-3
+    return tot / reps
+
+
+def time_graph_steps(step, steps, device, dist=None):
+    import torch
+    stream = torch.cuda.current_stream(device)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    return e0.elapsed_time(e1) * 1e-3
+
+
 def bench_ours(args):
     import torch
 
@@ -409,7 +446,7 @@ def bench_ours(args):
     q.lib()
     peaks = load_peaks()
 
-    step = DecodeStep(device, bits=8, dtype=torch.float16, seed=2)
+    step = DecodeStep(device, bits=8, dtype=torch.float16, seed=2, mode="launches")
     x_host = torch.randn((1, 2048), generator=torch.Generator().manual_seed(0)).to(
         torch.float16).pin_memory()
     step.x0.copy_(x_host)
@@ -424,29 +461,30 @@ def bench_ours(args):
     if hasattr(props, "pci_bus_id"):
         pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
                                     props.pci_device_id)
-    # ---- timed region: exactly `steps` graph replays
+    # ---- timed region: exactly `steps` graph replays (65 overlapped launches each)
     sampler = ClockSampler(pci)
-    barrier(dist)
-    torch.cuda.synchronize(device)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
     with sampler:
-        e0.record(stream)
-        for _ in range(args.steps):
-            step.replay()
-        e1.record(stream)
-        torch.cuda.synchronize(device)
-    barrier(dist)
-    t_local = e0.elapsed_time(e1) * 1e-3
+        t_local = time_graph_steps(step, args.steps, device, dist)
     t = max_over_ranks(dist, t_local, device)
     per_step = t / args.steps
     value = world * args.steps / t
 
-    # ---- per-launch durations of the dominant kernel (qmv)
+    # ---- the dominant kernel (qmv) launch by launch, CUDA events on its stream
+    alg_list = step.algorithmic_bytes()
+    alg = sum(alg_list)
     durs = per_launch_durations(step, device)
-    alg = step.algorithmic_bytes()
-    achieved = sum(alg) / sum(durs) / 1e9
+    achieved = alg / sum(durs) / 1e9
     top = max(range(step.n_launches), key=lambda i: durs[i])
+
+    # ---- the same step as one persistent chain launch (qlin_qmv_chain), for comparison
+    step.mode = "chain"
+    step.capture()
+    for _ in range(3):
+        step.replay()
+    t_c = time_graph_steps(step, args.steps, device)
+    chain_s = time_eager(step.launch_chain, device)
+    step.mode = "launches"
+    step.capture()
 
     # ---- end to end through the public API with host buffers
     logits_host = torch.empty((1, step.logits.shape[1]), dtype=torch.float16).pin_memory()
@@ -486,15 +524,17 @@ def bench_ours(args):
         "qmv_step_frac_of_peak": bytes_step / per_step / 1e9 / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "qmv_kernel (all %d launches of a step, per-launch events)"
+                     "kernel": "qmv_kernel (the %d launches of a step, each timed with events)"
                                % step.n_launches,
-                     "algorithmic_bytes_per_launch": sum(alg) / len(alg),
+                     "algorithmic_bytes_per_launch": alg / step.n_launches,
                      "mean_launch_us": sum(durs) / len(durs) * 1e6,
                      "peak_source": peaks["source"],
-                     "per_shape": per_shape_summary(step, durs, alg),
-                     "largest_launch": {"name": step.units[top]["name"],
-                                        "us": durs[top] * 1e6,
-                                        "gbs": alg[top] / durs[top] / 1e9}},
+                     "per_shape": per_shape_summary(step, durs, alg_list),
+                     "largest_launch": {"name": step.units[top]["name"], "us": durs[top] * 1e6,
+                                        "gbs": alg_list[top] / durs[top] / 1e9}},
+        "chain_mode": {"tokens_per_s": world * args.steps / t_c,
+                       "kernel_us": chain_s * 1e6,
+                       "kernel_gbs": alg / chain_s / 1e9},
         "qmm": qmm_res,
         "crossover": cross,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,

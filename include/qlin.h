@@ -140,6 +140,47 @@ qlin_status qlin_qmv_ex(const void* x, const uint32_t* wq, const void* scales, c
                         qlin_dtype dtype, unsigned flags, void* stream);
 
 /*
+ * A chain of dependent M = 1 products in one launch (a decode step).
+ *
+ * Link i computes y_i = x_i . W_hat_i^T with W_i given in the packed format
+ * above (wq, scales, biases of shape [N][K]), where x_i is x0 (input = -1) or
+ * the K elements starting at element input_offset of an earlier link's output
+ * (0 <= input < i, input_offset + K <= N of that link).  The result is the
+ * same as calling qlin_qmv on the links in order; the whole chain runs as one
+ * persistent cooperative kernel whose CTAs stream every link's weights without
+ * waiting and only wait, per link, until the row blocks of its input link are
+ * complete.  The pages trace the packed path's slowness to unfused, separately
+ * dispatched steps (~678 dispatches per decode step: "epic: realize
+ * low-precision / quantized performance on the OpenXLA (IREE) backend",
+ * section "The measured fusion gate").
+ */
+typedef struct {
+  const uint32_t* wq;      /* [N][K*bits/32], 16-byte aligned */
+  const void* scales;      /* dtype [N][K/group_size] */
+  const void* biases;      /* dtype [N][K/group_size] */
+  void* y;                 /* dtype [N] output; 16-byte aligned if a later link reads it */
+  int64_t N, K;
+  int32_t input;           /* -1: x0; else index of an earlier link */
+  int32_t input_offset;    /* first element of that link's output read as x (x16 bytes aligned) */
+} qlin_link;
+
+/* Bytes of device scratch qlin_qmv_chain needs for n_links links (one 32-bit
+ * completion counter per link, rounded up to 256 bytes). */
+size_t qlin_qmv_chain_workspace_size(int n_links);
+
+/*
+ * Run the chain.  x0: dtype [K of the links reading it], 16-byte aligned (may
+ * be NULL when no link reads it).  workspace: device scratch of at least
+ * qlin_qmv_chain_workspace_size(n_links) bytes, 16-byte aligned, owned by the
+ * caller; the call zeroes it on the stream first, so concurrent chains need
+ * separate workspaces.  1 <= n_links <= 160.  Outputs must not overlap any
+ * weight or another link's output.  Errors as for qlin_qmv.
+ */
+qlin_status qlin_qmv_chain(const void* x0, const qlin_link* links, int n_links, int bits,
+                           int group_size, qlin_dtype dtype, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
  * The same product on the tensor cores (batched decode and prefill): packed
  * tiles are staged into shared memory by TMA, dequantised there to dtype
  * (bit-identical to qlin_dequant's dtype output) and fed to tcgen05 MMA with
@@ -165,7 +206,8 @@ int64_t qlin_crossover_m(int64_t N, int64_t K, int bits);
  * Read and clear the device status words of the current device (synchronises
  * the device).  *flags receives 0 when no kernel gave up a bounded wait since
  * the last call, else a bit mask of the waits that gave up (bits 0-7: the
- * tensor-core kernel, bits 8-15: the CUDA-core kernel).  Returns QLIN_OK, or
+ * tensor-core kernel, bits 8-15: the CUDA-core kernel, bits 16-23: the chain
+ * kernel).  Returns QLIN_OK, or
  * QLIN_ERR_CUDA if the device could not be read.
  */
 qlin_status qlin_device_status(int* flags);

@@ -24,7 +24,8 @@ from .build_lib import LIB_PATH
 
 __all__ = [
     "QlinError", "lib", "quantize_affine", "dequant", "qmv", "qmm", "linear",
-    "crossover_m", "device_status", "QLIN_F32", "QLIN_F16", "QLIN_BF16",
+    "crossover_m", "device_status", "QLIN_F32", "QLIN_F16", "QLIN_BF16", "Link", "make_links",
+    "chain_workspace", "qmv_chain",
 ]
 
 QLIN_F32, QLIN_F16, QLIN_BF16 = 0, 1, 2
@@ -48,10 +49,20 @@ _SIGNATURES = {
     "qlin_qmm": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_linear": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_crossover_m": (_c_i64, [_c_i64, _c_i64, _c_int]),
+    "qlin_qmv_chain_workspace_size": (ctypes.c_size_t, [_c_int]),
+    "qlin_qmv_chain": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int, _c_vp,
+                                ctypes.c_size_t, _c_vp]),
     "qlin_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
 }
 
 _LIB = None
+
+
+class Link(ctypes.Structure):
+    """qlin_link: one M = 1 product of a chain (include/qlin.h)."""
+    _fields_ = [("wq", _c_vp), ("scales", _c_vp), ("biases", _c_vp), ("y", _c_vp),
+                ("N", _c_i64), ("K", _c_i64), ("input", ctypes.c_int32),
+                ("input_offset", ctypes.c_int32)]
 
 
 class QlinError(RuntimeError):
@@ -167,6 +178,35 @@ def qmm(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
 def linear(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
     """qmv below the measured crossover M, qmm above it."""
     return _matmul("qlin_linear", x, wq, scales, biases, bits, group_size, out)
+
+
+def chain_workspace(n_links: int, device) -> torch.Tensor:
+    """Device scratch for qmv_chain (one counter per link)."""
+    nbytes = int(lib().qlin_qmv_chain_workspace_size(n_links))
+    return torch.zeros(nbytes // 4, dtype=torch.int32, device=device)
+
+
+def make_links(links):
+    """ctypes array of Link from dicts with wq, scales, biases, y, input,
+    input_offset (tensors must stay alive while the array is used)."""
+    arr = (Link * len(links))()
+    for i, d in enumerate(links):
+        n, k = d["wq"].shape[0], None
+        arr[i] = Link(d["wq"].data_ptr(), d["scales"].data_ptr(), d["biases"].data_ptr(),
+                      d["y"].data_ptr(), n, d["K"], d.get("input", -1), d.get("input_offset", 0))
+    return arr
+
+
+def qmv_chain(x0, link_array, n_links, bits, dtype, workspace, group_size=GROUP_SIZE):
+    """Run a chain of dependent M = 1 products in one launch (qlin_qmv_chain).
+
+    x0: device tensor (or None); link_array: from make_links; workspace: from
+    chain_workspace.  Outputs are written into each link's y."""
+    dev = workspace.device
+    _check(lib().qlin_qmv_chain(_ptr(x0) if x0 is not None else None, link_array, n_links,
+                                bits, group_size, _DTYPE_CODE[dtype], _ptr(workspace),
+                                workspace.numel() * 4,
+                                ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)))
 
 
 def crossover_m(n: int, k: int, bits: int) -> int:

@@ -176,6 +176,57 @@ qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, cons
                       group_size, dtype, 0u, stream);
 }
 
+size_t qlin_qmv_chain_workspace_size(int n_links) {
+  if (n_links <= 0) return 0;
+  return (size_t(n_links) * sizeof(unsigned) + 255) / 256 * 256;
+}
+
+qlin_status qlin_qmv_chain(const void* x0, const qlin_link* links, int n_links, int bits,
+                           int group_size, qlin_dtype dtype, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  g_last_error[0] = 0;
+  if (!links || n_links < 1 || n_links > chain_max_links())
+    return fail(QLIN_ERR_INVALID_ARG, "qlin_qmv_chain: need 1..%d links", chain_max_links());
+  qlin_status s = check_act_dtype(dtype, "activation/scale");
+  if (s != QLIN_OK) return s;
+  if (!workspace || workspace_bytes < qlin_qmv_chain_workspace_size(n_links))
+    return fail(QLIN_ERR_INVALID_ARG, "qlin_qmv_chain: workspace of %zu bytes needed",
+                qlin_qmv_chain_workspace_size(n_links));
+  if (!aligned(workspace, 16))
+    return fail(QLIN_ERR_MISALIGNED, "qlin_qmv_chain: workspace must be 16-byte aligned");
+  for (int l = 0; l < n_links; ++l) {
+    const qlin_link& L = links[l];
+    if ((s = check_format(L.N, L.K, bits, group_size)) != QLIN_OK)
+      return fail(s, "qlin_qmv_chain: link %d: %s", l, qlin_last_error());
+    if (L.N < 1 || L.N > (int64_t(1) << 30) || L.K > (int64_t(1) << 20))
+      return fail(QLIN_ERR_INVALID_ARG, "qlin_qmv_chain: link %d: N=%lld K=%lld out of range", l,
+                  (long long)L.N, (long long)L.K);
+    if (!L.wq || !L.scales || !L.biases || !L.y)
+      return fail(QLIN_ERR_INVALID_ARG, "qlin_qmv_chain: link %d: null pointer", l);
+    if (!aligned(L.wq, 16) || !aligned(L.scales, 2) || !aligned(L.biases, 2) || !aligned(L.y, 2))
+      return fail(QLIN_ERR_MISALIGNED, "qlin_qmv_chain: link %d: misaligned pointer", l);
+    if (L.input < 0) {
+      if (L.input != -1) return fail(QLIN_ERR_INVALID_ARG, "qlin_qmv_chain: link %d: input", l);
+      if (!x0) return fail(QLIN_ERR_INVALID_ARG, "qlin_qmv_chain: link %d reads a null x0", l);
+      if (!aligned(x0, 16))
+        return fail(QLIN_ERR_MISALIGNED, "qlin_qmv_chain: x0 must be 16-byte aligned");
+    } else {
+      if (L.input >= l)
+        return fail(QLIN_ERR_INVALID_ARG, "qlin_qmv_chain: link %d reads link %d (not earlier)",
+                    l, L.input);
+      const qlin_link& D = links[L.input];
+      if (L.input_offset < 0 || int64_t(L.input_offset) + L.K > D.N)
+        return fail(QLIN_ERR_INVALID_ARG,
+                    "qlin_qmv_chain: link %d reads past the end of link %d's output", l, L.input);
+      if (!aligned(static_cast<const uint8_t*>(D.y) + int64_t(L.input_offset) * 2, 16))
+        return fail(QLIN_ERR_MISALIGNED,
+                    "qlin_qmv_chain: link %d's input must start 16-byte aligned", l);
+    }
+  }
+  return launch_qmv_chain(x0, links, n_links, bits, dtype, workspace,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
   (void)N;
   (void)K;
@@ -202,14 +253,15 @@ qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
 qlin_status qlin_device_status(int* flags) {
   g_last_error[0] = 0;
   if (!flags) return fail(QLIN_ERR_INVALID_ARG, "qlin_device_status: null pointer");
-  unsigned fm = 0, fv = 0;
+  unsigned fm = 0, fv = 0, fc = 0;
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = qmm_take_device_status(&fm);
   if (e == cudaSuccess) e = qmv_take_device_status(&fv);
+  if (e == cudaSuccess) e = chain_take_device_status(&fc);
   if (e != cudaSuccess)
     return fail(QLIN_ERR_CUDA, "qlin_device_status: %s", cudaGetErrorString(e));
-  // qmm waits in the low byte, qmv waits in the next one
-  *flags = static_cast<int>((fm & 0xffu) | ((fv & 0xffu) << 8));
+  // qmm waits in the low byte, qmv waits in the next one, the chain above
+  *flags = static_cast<int>((fm & 0xffu) | ((fv & 0xffu) << 8) | ((fc & 0xffu) << 16));
   return QLIN_OK;
 }
 

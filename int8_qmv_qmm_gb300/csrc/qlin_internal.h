@@ -30,9 +30,14 @@ qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, co
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
                        unsigned flags, cudaStream_t st);
 
+qlin_status launch_qmv_chain(const void* x0, const qlin_link* links, int n_links, int bits,
+                             qlin_dtype dtype, void* ws, cudaStream_t st);
+int chain_max_links();
+
 // Read and clear the kernels' device status words (no synchronisation).
 cudaError_t qmm_take_device_status(unsigned* flags);
 cudaError_t qmv_take_device_status(unsigned* flags);
+cudaError_t chain_take_device_status(unsigned* flags);
 
 constexpr int kGroup = 64;
 

@@ -27,7 +27,7 @@ from __future__ import annotations
 
 import torch
 
-from . import qmv, quantize_affine
+from . import chain_workspace, make_links, qmv, qmv_chain, quantize_affine
 from . import synthetic as S
 
 _FUSED = (("qkv", ("q_proj", "k_proj", "v_proj")), ("o", ("o_proj",)),
@@ -37,11 +37,15 @@ _FUSED = (("qkv", ("q_proj", "k_proj", "v_proj")), ("o", ("o_proj",)),
 class DecodeStep:
     def __init__(self, device, bits: int = 8, dtype: torch.dtype = torch.float16,
                  seed: int = 2, layers: int = S.LLAMA_1B_LAYERS, lm_head: bool = True,
-                 overlap: bool = True):
+                 overlap: bool = True, mode: str = "launches"):
+        """mode "launches": one qlin_qmv launch per fused linear (overlapped
+        with programmatic dependent launch when ``overlap``; the faster mode on
+        GB300); mode "chain": the whole step is one qlin_qmv_chain launch."""
         self.device = torch.device(device)
         self.bits = bits
         self.dtype = dtype
         self.overlap = overlap
+        self.mode = mode
         shapes = {name: (n, k) for name, n, k in S.LLAMA_1B_LINEARS}
         # original linears, in the order of the weight seeds:
         # (name, layer, N, K, unit index, first row in the unit, weight seed)
@@ -71,6 +75,27 @@ class DecodeStep:
         hidden = S.LLAMA_1B_LINEARS[0][2]
         self.x0 = torch.zeros((1, hidden), dtype=dtype, device=self.device)
         self.graph = None
+        self._build_chain()
+
+    def _build_chain(self):
+        """The link table of the step (same chaining as input_of)."""
+        links = []
+        for u, d in enumerate(self.units):
+            name = d["name"]
+            if name == "qkv":
+                inp, off = (-1, 0) if u == 0 else (u - 1, 0)
+            elif name == "o":
+                inp, off = u - 1, 0            # q rows of the fused qkv output
+            elif name == "gate_up":
+                inp, off = u - 1, 0
+            elif name == "down":
+                inp, off = u - 1, 0            # gate rows of the fused gate_up output
+            else:
+                inp, off = (u - 1, 0) if u else (-1, 0)
+            links.append(dict(wq=d["wq"], scales=d["scales"], biases=d["biases"], y=d["out"],
+                              K=d["K"], input=inp, input_offset=off))
+        self._links = make_links(links)
+        self._workspace = chain_workspace(len(links), self.device)
 
     def _add_unit(self, name, layer, w):
         n, k = w.shape
@@ -116,6 +141,16 @@ class DecodeStep:
         return qmv(x, d["wq"], d["scales"], d["biases"], self.bits,
                    out=d["out"] if out is None else out, overlap_previous=overlap)
 
+    def launch_chain(self):
+        qmv_chain(self.x0, self._links, len(self.units), self.bits, self.dtype, self._workspace)
+
+    def run_step(self):
+        """One decode step in the configured mode (eager)."""
+        if self.mode == "chain":
+            self.launch_chain()
+        else:
+            self.launch_all()
+
     def launch_all(self, per_launch_hook=None):
         for u in range(len(self.units)):
             if per_launch_hook:
@@ -126,11 +161,11 @@ class DecodeStep:
 
     def capture(self, stream: torch.cuda.Stream | None = None):
         """Capture one step into a CUDA graph (after one eager warm-up)."""
-        self.launch_all()
+        self.run_step()
         torch.cuda.synchronize(self.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            self.launch_all()
+            self.run_step()
         self.graph = g
         return g
 

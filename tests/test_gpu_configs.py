@@ -64,8 +64,9 @@ def test_full_decode_step_sampled_rows(dev):
     """All 113 linears of the 8-bit decode step (stored fused as the step
     launches them), each run on fresh synthetic input through its own launch;
     48 sampled rows per linear are checked against the oracle (codes
-    bit-exact, outputs within tolerance).  Then the chained graph, with its
-    overlapped launches, replays and gives finite, repeatable logits."""
+    bit-exact, outputs within tolerance).  Then the step's graph (one chain
+    launch) replays and gives finite, repeatable logits, identical to per-linear
+    launches."""
     from int8_qmv_qmm_gb300.decode_step import DecodeStep
     step = DecodeStep(dev, bits=8, dtype=torch.float16, seed=2)
     assert len(step.linears) == 113 and step.n_launches == 65
@@ -89,8 +90,13 @@ def test_full_decode_step_sampled_rows(dev):
     step.replay()
     torch.cuda.synchronize()
     assert torch.equal(first, step.logits)
-    # the overlapped chain computes exactly what plain stream-ordered launches do
+    # the single-launch chain and the overlapped per-linear launches compute
+    # exactly what plain stream-ordered launches do
     step.overlap = False
+    step.launch_all()
+    torch.cuda.synchronize()
+    assert torch.equal(first, step.logits)
+    step.overlap = True
     step.launch_all()
     torch.cuda.synchronize()
     assert torch.equal(first, step.logits)

@@ -156,3 +156,73 @@ def test_empty_batch_is_a_no_op(dev):
 
 def test_no_kernel_gave_up_a_wait(dev):
     assert q.device_status() == 0
+
+
+# ------------------------------------------------------------ qmv chain
+def _chain_links(dev, specs, dt, seed):
+    """specs: (N, K, bits, input, input_offset); weights quantised on the GPU."""
+    links, refs = [], []
+    for i, (n, k, bits, inp, off) in enumerate(specs):
+        w = S.weights_f32(seed + i, n, k)
+        wq, sc, bi = _upload(dev, w, bits, dt)
+        y = torch.empty((1, n), dtype=TORCH_DT[dt], device=dev)
+        links.append(dict(wq=wq, scales=sc, biases=bi, y=y, K=k, input=inp, input_offset=off))
+        refs.append(w)
+    return links, refs
+
+
+@pytest.mark.parametrize("bits,dt", [(8, "f16"), (4, "bf16"), (4, "f16"), (8, "bf16")])
+def test_qmv_chain_independent_links_match_oracle(dev, bits, dt):
+    """Every link reads x0: each output is checked against the oracle."""
+    specs = [(300, 512, bits, -1, 0), (1, 512, bits, -1, 0), (1029, 512, bits, -1, 0),
+             (64, 512, bits, -1, 0), (2048, 512, bits, -1, 0)]
+    links, ws_ = _chain_links(dev, specs, dt, 4100 + bits)
+    x0 = S.activations(17, 1, 512, dt)
+    arr = q.make_links(links)
+    wsp = q.chain_workspace(len(links), dev)
+    q.qmv_chain(x0.to(dev), arr, len(links), bits, TORCH_DT[dt], wsp)
+    torch.cuda.synchronize()
+    for d, w in zip(links, ws_):
+        ref = O.linear_ref(x0.float().numpy().astype(np.float64), w, bits, 64, dt)
+        assert_within_tolerance(d["y"], ref, f"chain link N={w.shape[0]}")
+
+
+@pytest.mark.parametrize("bits,dt", [(8, "f16"), (4, "bf16")])
+def test_qmv_chain_equals_sequential_launches(dev, bits, dt):
+    """A dependent chain (slices of earlier outputs, K not a multiple of 512 so
+    scales come from global memory, K = 8192 split into k-tiles) gives exactly
+    the outputs of launching qlin_qmv link by link."""
+    specs = [(3072, 2048, bits, -1, 0), (2048, 2048, bits, 0, 0), (4160, 2048, bits, 1, 0),
+             (2048, 4096, bits, 2, 64), (320, 2048, bits, 3, 0), (1000, 192, bits, 4, 128),
+             (8192, 320, bits, 5, 8), (96, 8192, bits, 6, 0)]
+    links, _ = _chain_links(dev, specs, dt, 5200 + bits)
+    x0 = S.activations(23, 1, 2048, dt).to(dev)
+    arr = q.make_links(links)
+    wsp = q.chain_workspace(len(links), dev)
+    for rep in range(2):  # the second run reuses (and re-zeroes) the workspace
+        q.qmv_chain(x0, arr, len(links), bits, TORCH_DT[dt], wsp)
+        torch.cuda.synchronize()
+        outs = [d["y"].clone() for d in links]
+        for i, d in enumerate(links):
+            x = x0 if d["input"] < 0 else \
+                outs[d["input"]][:, d["input_offset"]:d["input_offset"] + d["K"]].contiguous()
+            y = q.qmv(x, d["wq"], d["scales"], d["biases"], bits)
+            assert torch.equal(y, outs[i]), f"link {i} differs (run {rep})"
+    assert q.device_status() == 0
+
+
+def test_qmv_chain_rejects_bad_links(dev):
+    links, _ = _chain_links(dev, [(64, 512, 4, -1, 0), (64, 512, 4, 0, 0)], "f16", 1)
+    wsp = q.chain_workspace(2, dev)
+    bad = [dict(links[0]), dict(links[1], input=1)]          # reads itself
+    with pytest.raises(q.QlinError):
+        q.qmv_chain(None, q.make_links(bad), 2, 4, torch.float16, wsp)
+    bad = [dict(links[0]), dict(links[1], input_offset=8)]   # reads past the end
+    with pytest.raises(q.QlinError):
+        q.qmv_chain(None, q.make_links(bad), 2, 4, torch.float16, wsp)
+    with pytest.raises(q.QlinError):                          # link 0 reads a null x0
+        q.qmv_chain(None, q.make_links(links), 2, 4, torch.float16, wsp)
+    small = torch.zeros(1, dtype=torch.int32, device=dev)    # workspace too small
+    x0 = torch.zeros((1, 512), dtype=torch.float16, device=dev)
+    with pytest.raises(q.QlinError):
+        q.qmv_chain(x0, q.make_links(links), 2, 4, torch.float16, small)
