@@ -181,6 +181,27 @@ qlin_status qlin_qmv_chain(const void* x0, const qlin_link* links, int n_links, 
                            size_t workspace_bytes, void* stream);
 
 /*
+ * qlin_qmv_chain for callers that cannot allocate device memory (no
+ * counterpart on the pages; an addition of this library).
+ *
+ * Same chain, same arguments and same results as qlin_qmv_chain, but the
+ * per-link scratch counters live in a file-scope static device array inside
+ * the library, so the call allocates nothing: for plugins whose host
+ * framework owns all device memory through its own pool and forbids
+ * cudaMalloc, and for deployments whose device memory budget is fixed at
+ * start-up.  Limits: at most QLIN_CHAIN_STATIC_MAX_LINKS links (larger counts
+ * return QLIN_ERR_INVALID_ARG); every GPU that loads the library keeps its
+ * copy of the array until the process exits; all calls on a device share it
+ * (each call zeroes the counters it uses on its stream first), so calls whose
+ * kernels overlap on the GPU race and give wrong results.  The first call on
+ * each device looks up the array's device address; make it before any stream
+ * capture.
+ */
+#define QLIN_CHAIN_STATIC_MAX_LINKS 160
+qlin_status qlin_qmv_chain_static(const void* x0, const qlin_link* links, int n_links, int bits,
+                                  int group_size, qlin_dtype dtype, void* stream);
+
+/*
  * The same product on the tensor cores (batched decode and prefill): packed
  * tiles are staged into shared memory by TMA, dequantised there to dtype
  * (bit-identical to qlin_dequant's dtype output) and fed to tcgen05 MMA with

@@ -52,6 +52,7 @@ _SIGNATURES = {
     "qlin_qmv_chain_workspace_size": (ctypes.c_size_t, [_c_int]),
     "qlin_qmv_chain": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int, _c_vp,
                                 ctypes.c_size_t, _c_vp]),
+    "qlin_qmv_chain_static": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int, _c_vp]),
     "qlin_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
 }
 

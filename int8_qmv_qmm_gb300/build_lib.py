@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libqlin.so")
 
-SOURCES = ("api.cu", "quant.cu", "qmv.cu", "qmv_chain.cu", "qmm.cu")
+SOURCES = ("api.cu", "quant.cu", "qmv.cu", "qmv_chain.cu", "chain_static.cu", "qmm.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [
     "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
