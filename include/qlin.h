@@ -99,8 +99,9 @@ qlin_status qlin_quantize_affine(const float* w, int64_t N, int64_t K, int bits,
 /*
  * Materialise the reconstruction w_hat[N][K] = RNE_out(q*scale + bias): one
  * correctly rounded step from the exact value, so it is bit-identical to a
- * host dequantisation ("What is already in-tree": in-graph reconstruction is
- * bit-identical to the host dequant).  out_dtype: QLIN_F32, or equal to
+ * host dequantisation (the pages require the in-graph reconstruction to match
+ * the host dequant exactly: "track(upstream-iree): ...", section "What is
+ * already in-tree").  out_dtype: QLIN_F32, or equal to
  * sdtype.  This is the unfused reference path and a test carrier; the matmul
  * entry points below never call it.  Alignment: wq and w_out 16-byte aligned.
  */

@@ -22,8 +22,8 @@ Sources (web pages on the method; cited by page title and section):
       dequantised in the graph.
   [mlxcel-574 in-tree]  "track(upstream-iree): fused dequant->matmul for the
       packed int8 bandwidth win", section "What is already in-tree": bit-unpack,
-      then q*scale + bias; the in-graph reconstruction is bit-identical to the
-      host dequant; bf16 scales/biases are accepted by the dequant path.
+      then q*scale + bias; the reconstruction inside the graph matches a host
+      dequantisation bit for bit; bf16 scales/biases are accepted.
   [mlxcel-574 blocker]  same page, section "The blocker (measured)": the
       reconstructed weight must not be materialised; the matmul consumes it.
   [executorch-17187]    "Metal backend: import qmv_impl from MLX": the M=1
