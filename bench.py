@@ -584,7 +584,8 @@ def profile_case(which: str, launches: int = 3):
     dev = torch.device("cuda", 0)
     cases = {"qmv": (1, 128256, 2048, 8, q.qmv), "qmv_o": (1, 2048, 2048, 8, q.qmv),
              "qmv_gate_up": (1, 16384, 2048, 8, q.qmv), "qmv_down": (1, 2048, 8192, 8, q.qmv),
-             "qmm": (2048, 8192, 2048, 4, q.qmm)}
+             "qmm": (2048, 8192, 2048, 4, q.qmm), "qmm8": (2048, 8192, 2048, 8, q.qmm),
+             "qmm_sq": (2048, 2048, 2048, 8, q.qmm)}
     m, n, k, bits, fn = cases[which]
     w = torch.from_numpy(S.weights_f32(7, n, k)).to(dev)
     wq, sc, bi = q.quantize_affine(w, bits, sdtype=torch.float16)
@@ -609,7 +610,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-qmm", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["qmv", "qmv_o", "qmv_gate_up", "qmv_down", "qmm"],
+    ap.add_argument("--profile", choices=["qmv", "qmv_o", "qmv_gate_up", "qmv_down", "qmm",
+                                          "qmm8", "qmm_sq"],
                     help="run a small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:

@@ -228,15 +228,16 @@ qlin_status qlin_qmv_chain(const void* x0, const qlin_link* links, int n_links, 
 }
 
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
-  (void)N;
-  (void)K;
   (void)bits;
   const char* env = getenv("QLIN_CROSSOVER_M");
   if (env && *env) {
     long long v = atoll(env);
     if (v >= 1) return v;
   }
-  return 2;
+  // Measured on GB300 (batched-decode sweep, 4-bit, bf16, L2 flushed): the
+  // tensor-core kernel overtakes the CUDA-core one at M = 8 when N >= K
+  // (8192 x 2048) and at M = 16 when K > N (2048 x 8192).
+  return K > N ? 16 : 8;
 }
 
 qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,

@@ -47,7 +47,7 @@ namespace {
 
 constexpr int kBM = 128;          // weight rows per tile (MMA M)
 constexpr int kBK = 64;           // k per stage (one group)
-constexpr int kThreads = 192;     // 6 warps
+constexpr int kThreads = 14 * 32;  // TMA, MMA, 8 dequant, 4 epilogue warps
 
 enum : unsigned {
   kStatusProducer = 1u,
@@ -73,9 +73,13 @@ struct Layout {
   static constexpr int kXBytes = BN * kBK * 2;           // x tile, 128-byte rows
   static constexpr int kABytes = kBM * kBK * 2;          // dequantised tile
   static constexpr int kWBytes = Geo<BITS>::kPackedBytes;
-  static constexpr int kStageBytes = round_up(kXBytes, 1024) + kABytes + round_up(kWBytes, 1024);
+  static constexpr int kSBytes = 2 * kBM * 16;           // 8 groups of scales + of biases
+  static constexpr int kXOff = round_up(kXBytes, 1024);
+  static constexpr int kWOff = kXOff + kABytes;
+  static constexpr int kSOff = kWOff + round_up(kWBytes, 1024);
+  static constexpr int kStageBytes = kSOff + round_up(kSBytes, 1024);
   static constexpr int kTxBytes = kXBytes + kWBytes;
-  static constexpr uint32_t kTmemCols = BN < 32 ? 32 : BN;
+  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
 };
 
 // ---- unpack + dequantise one 16-bit pair: returns (w_hat[2j], w_hat[2j+1])
@@ -145,9 +149,10 @@ __device__ __forceinline__ uint32_t splat(AT v) {
   return uint32_t(u) | (uint32_t(u) << 16);
 }
 
-template <int BITS, typename AT, int BN>
+template <int BITS, typename AT, int BN, bool SCALE_TMA>
 __global__ void __launch_bounds__(kThreads, 1)
     qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+               const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
                const AT* __restrict__ scales, const AT* __restrict__ biases, AT* __restrict__ y,
                int M, int N, int K, int stages) {
   using L = Layout<BITS, BN>;
@@ -158,33 +163,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const gbase = smem_raw + (base - raw_base);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBM, m0 = blockIdx.y * BN;
   const int kb_count = K / kBK;
+  const int n_tiles = (N + kBM - 1) / kBM, m_tiles = (M + BN - 1) / BN;
+  const int total_tiles = n_tiles * m_tiles;
 
-  // stage s: [x tile][A tile][packed tile]
+  // stage s: [x tile][A tile][packed tile][scales][biases]
   auto x_addr = [&](int s) { return base + uint32_t(s * L::kStageBytes); };
-  auto a_addr = [&](int s) { return x_addr(s) + uint32_t(round_up(L::kXBytes, 1024)); };
-  auto w_addr = [&](int s) { return a_addr(s) + uint32_t(L::kABytes); };
+  auto a_addr = [&](int s) { return x_addr(s) + uint32_t(L::kXOff); };
+  auto w_addr = [&](int s) { return x_addr(s) + uint32_t(L::kWOff); };
+  auto s_addr = [&](int s) { return x_addr(s) + uint32_t(L::kSOff); };
   const uint32_t bar_base = base + uint32_t(stages * L::kStageBytes);
   auto full_bar = [&](int s) { return bar_base + 8u * s; };
   auto empty_bar = [&](int s) { return bar_base + 8u * (stages + s); };
   auto afull_bar = [&](int s) { return bar_base + 8u * (2 * stages + s); };
-  const uint32_t acc_bar = bar_base + 8u * (3 * stages);
-  const uint32_t done_bar = acc_bar + 8u;
+  const uint32_t accf_bar = bar_base + 8u * (3 * stages);   // [2] MMA -> epilogue
+  const uint32_t acce_bar = accf_bar + 16u;                   // [2] epilogue -> MMA
+  const uint32_t done_bar = acce_bar + 16u;
   const uint32_t tmem_slot = done_bar + 8u;
   uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(gbase + (tmem_slot - base));
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), 1 + 4);  // MMA commit + one per dequant warp
-      ptx::mbar_init(afull_bar(s), 4);      // one per dequant warp
+      ptx::mbar_init(empty_bar(s), 1 + 4);  // MMA commit + the 4 warps of the dequant group
+      ptx::mbar_init(afull_bar(s), 4);
     }
-    ptx::mbar_init(acc_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(accf_bar + 8u * b, 1);
+      ptx::mbar_init(acce_bar + 8u * b, 4);  // the epilogue warps
+    }
     ptx::mbar_init(done_bar, 1);
     ptx::fence_mbar_init();
     ptx::tma_prefetch_desc(&tm_x);
     ptx::tma_prefetch_desc(&tm_w);
+    if constexpr (SCALE_TMA) {
+      ptx::tma_prefetch_desc(&tm_s);
+      ptx::tma_prefetch_desc(&tm_b);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, L::kTmemCols);
@@ -195,29 +210,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
 
-  bool ok = true;
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < kb_count; ++kb) {
-        const int s = kb % stages;
-        const uint32_t round = uint32_t(kb / stages);
-        if (kb >= stages && !ptx::mbar_wait(empty_bar(s), (round - 1) & 1u)) {
-          report(kStatusProducer);
-          ok = false;
-          break;
+      int s = 0, issued = 0;
+      uint32_t round = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const int n0 = (t % n_tiles) * kBM, m0 = (t / n_tiles) * BN;
+        for (int kb = 0; kb < kb_count; ++kb) {
+          if (round > 0 && !ptx::mbar_wait(empty_bar(s), (round - 1) & 1u)) {
+            report(kStatusProducer);
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(full_bar(s), L::kTxBytes + (SCALE_TMA ? L::kSBytes : 0));
+          ptx::tma_load_2d(x_addr(s), &tm_x, full_bar(s), kb * kBK, m0);
+          ptx::tma_load_2d(w_addr(s), &tm_w, full_bar(s), kb * G::kWordsPerGroup, n0);
+          if constexpr (SCALE_TMA) {
+            // the 8 groups holding group kb (x coordinate a multiple of 8 groups = 16 bytes)
+            ptx::tma_load_2d(s_addr(s), &tm_s, full_bar(s), kb & ~7, n0);
+            ptx::tma_load_2d(s_addr(s) + uint32_t(kBM * 16), &tm_b, full_bar(s), kb & ~7, n0);
+          }
+          ++issued;
+          if (++s == stages) {
+            s = 0;
+            ++round;
+          }
         }
-        ptx::mbar_arrive_expect_tx(full_bar(s), L::kTxBytes);
-        ptx::tma_load_2d(x_addr(s), &tm_x, full_bar(s), kb * kBK, m0);
-        ptx::tma_load_2d(w_addr(s), &tm_w, full_bar(s), kb * G::kWordsPerGroup, n0);
-        ++issued;
       }
       if (!ok) {
-        // let the copies this CTA issued land before its shared memory goes away
         const int first = issued > stages ? issued - stages : 0;
-        for (int kb = first; kb < issued; ++kb)
-          if (!ptx::mbar_wait(full_bar(kb % stages), uint32_t(kb / stages) & 1u))
+        for (int v = first; v < issued; ++v)
+          if (!ptx::mbar_wait(full_bar(v % stages), uint32_t(v / stages) & 1u))
             report(kStatusTeardown);
       }
     }
@@ -226,129 +251,147 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t fmt = std::is_same<AT, __half>::value ? 0u : 1u;
       constexpr uint32_t idesc = ptx::idesc_f16(fmt, kBM, BN);
-      bool any = false;
-      for (int kb = 0; kb < kb_count; ++kb) {
-        const int s = kb % stages;
-        const uint32_t par = uint32_t(kb / stages) & 1u;
-        if (!ptx::mbar_wait(afull_bar(s), par) || !ptx::mbar_wait(full_bar(s), par)) {
+      int s = 0, i = 0;
+      uint32_t round = 0;
+      bool ok = true, any = false;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !ptx::mbar_wait(acce_bar + 8u * buf, uint32_t((i >> 1) - 1) & 1u)) {
           report(kStatusMma);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint64_t ad = ptx::sw128_kmajor_desc(a_addr(s));
-        const uint64_t bd = ptx::sw128_kmajor_desc(x_addr(s));
+        const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
+        for (int kb = 0; kb < kb_count; ++kb) {
+          if (!ptx::mbar_wait(afull_bar(s), round & 1u) || !ptx::mbar_wait(full_bar(s), round & 1u)) {
+            report(kStatusMma);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t ad = ptx::sw128_kmajor_desc(a_addr(s));
+          const uint64_t bd = ptx::sw128_kmajor_desc(x_addr(s));
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // +32 bytes along K = +2 in the descriptor's 16-byte address units
-          ptx::mma_f16_ss(tmem_base, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
-                          (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // +32 bytes along K = +2 in the descriptor's 16-byte address units
+            ptx::mma_f16_ss(d_tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
+                            (kb > 0 || kk > 0) ? 1u : 0u);
+          }
+          any = true;
+          ptx::mma_commit(empty_bar(s));
+          if (++s == stages) {
+            s = 0;
+            ++round;
+          }
         }
-        any = true;
-        ptx::mma_commit(empty_bar(s));
+        if (ok) ptx::mma_commit(accf_bar + 8u * buf);
       }
-      ptx::mma_commit(ok ? acc_bar : done_bar);
-      if (!ok && any && !ptx::mbar_wait(done_bar, 0)) report(kStatusTeardown);
+      // before TMEM is freed every MMA issued here must have completed
+      ptx::mma_commit(done_bar);
+      if (any && !ptx::mbar_wait(done_bar, 0)) report(kStatusTeardown);
+    }
+  } else if (warp < 2 + 8) {
+    // -------------------------------------------- dequantise (two groups)
+    const int grp = (warp - 2) >> 2;  // stages with (use index & 1) == grp
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // weight row within the tile
+    const int gpr = K / kGroup;
+    const int swz_a = r & 7;
+    int s = 0, u = 0;
+    uint32_t round = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      const int n = (t % n_tiles) * kBM + r;
+      const bool row_ok = n < N;
+      const AT* srow = scales + int64_t(min(n, N - 1)) * gpr;
+      const AT* brow = biases + int64_t(min(n, N - 1)) * gpr;
+      for (int kb = 0; kb < kb_count; ++kb, ++u) {
+        const int cs = s;
+        const uint32_t cround = round;
+        if (++s == stages) {
+          s = 0;
+          ++round;
+        }
+        if ((u & 1) != grp) continue;
+        AT sc, bc;
+        if constexpr (!SCALE_TMA) {
+          sc = srow[kb];
+          bc = brow[kb];
+        }
+        if (!ptx::mbar_wait(full_bar(cs), cround & 1u)) {
+          report(kStatusDequant);
+          ok = false;
+          break;
+        }
+        if constexpr (SCALE_TMA) {
+          const AT* ss = reinterpret_cast<const AT*>(gbase + (s_addr(cs) - base));
+          sc = ss[r * 8 + (kb & 7)];
+          bc = ss[kBM * 8 + r * 8 + (kb & 7)];
+        }
+        const uint32_t s2 = row_ok ? splat(sc) : 0u, b2 = row_ok ? splat(bc) : 0u;
+        const uint8_t* wrow = gbase + (w_addr(cs) - base) + r * G::kPackedRowBytes;
+        uint8_t* arow = gbase + (a_addr(cs) - base) + r * 128;
+        if constexpr (BITS == 4) {
+          // packed rows are 32 bytes in the 32-byte TMA swizzle: chunk c of row
+          // r sits at chunk c ^ ((r >> 2) & 1)
+          const int sw = (r >> 2) & 1;
+          const uint4 lo = *reinterpret_cast<const uint4*>(wrow + ((0 ^ sw) << 4));
+          const uint4 hi = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
+          const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(arow + ((c ^ swz_a) << 4)) =
+                dequant_word4<AT>(words[c], s2, b2);
+        } else {
+          // packed rows are 64 bytes in the 64-byte TMA swizzle: chunk c of row
+          // r sits at chunk c ^ ((r >> 1) & 3)
+          const int sw = (r >> 1) & 3;
+          uint32_t words[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ sw) << 4));
+            words[4 * c] = v.x;
+            words[4 * c + 1] = v.y;
+            words[4 * c + 2] = v.z;
+            words[4 * c + 3] = v.w;
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 o;
+            dequant_word8<AT>(words[2 * c], s2, b2, o.x, o.y);
+            dequant_word8<AT>(words[2 * c + 1], s2, b2, o.z, o.w);
+            *reinterpret_cast<uint4*>(arow + ((c ^ swz_a) << 4)) = o;
+          }
+        }
+        ptx::fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(afull_bar(cs));
+          ptx::mbar_arrive(empty_bar(cs));
+        }
+      }
     }
   } else {
-    // ------------------------------------------------ dequantise + epilogue
-    const int quarter = warp & 3;          // TMEM lane quarter this warp may access
-    const int r = quarter * 32 + lane;     // weight row within the tile
-    const int n = n0 + r;
-    const int gpr = K / kGroup;
-    const AT* srow = scales + int64_t(min(n, N - 1)) * gpr;
-    const AT* brow = biases + int64_t(min(n, N - 1)) * gpr;
-    const bool row_ok = n < N;
-    // scales/biases of the row, fetched 4 groups ahead of use
-    AT s_nxt[4], b_nxt[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      s_nxt[j] = j < gpr ? srow[j] : srow[0];
-      b_nxt[j] = j < gpr ? brow[j] : brow[0];
-    }
-    const int swz_a = r & 7;
-    for (int kb0 = 0; kb0 < kb_count && ok; kb0 += 4) {
-      AT s_cur[4], b_cur[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        s_cur[j] = s_nxt[j];
-        b_cur[j] = b_nxt[j];
-        if (kb0 + 4 + j < gpr) {
-          s_nxt[j] = srow[kb0 + 4 + j];
-          b_nxt[j] = brow[kb0 + 4 + j];
-        }
-      }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int kb = kb0 + j;
-      if (kb >= kb_count) break;
-      const int s = kb % stages;
-      const uint32_t par = uint32_t(kb / stages) & 1u;
-      const AT sc = s_cur[j], bc = b_cur[j];
-      if (!ptx::mbar_wait(full_bar(s), par)) {
-        report(kStatusDequant);
-        ok = false;
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;
+    int i = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
+      const int buf = i & 1;
+      if (!ptx::mbar_wait(accf_bar + 8u * buf, uint32_t(i >> 1) & 1u)) {
+        report(kStatusEpilogue);
         break;
       }
-      const uint32_t s2 = row_ok ? splat(sc) : 0u, b2 = row_ok ? splat(bc) : 0u;
-      const uint8_t* wrow = gbase + (w_addr(s) - base) + r * G::kPackedRowBytes;
-      uint8_t* arow = gbase + (a_addr(s) - base) + r * 128;
-      if constexpr (BITS == 4) {
-        // packed rows are 32 bytes in the 32-byte TMA swizzle: chunk c of row
-        // r sits at chunk c ^ ((r >> 2) & 1)
-        const int sw = (r >> 2) & 1;
-        const uint4 lo = *reinterpret_cast<const uint4*>(wrow + ((0 ^ sw) << 4));
-        const uint4 hi = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
-        const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(arow + ((c ^ swz_a) << 4)) =
-              dequant_word4<AT>(words[c], s2, b2);
-      } else {
-        // packed rows are 64 bytes in the 64-byte TMA swizzle: chunk c of row
-        // r sits at chunk c ^ ((r >> 1) & 3)
-        const int sw = (r >> 1) & 3;
-        uint32_t words[16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ sw) << 4));
-          words[4 * c] = v.x;
-          words[4 * c + 1] = v.y;
-          words[4 * c + 2] = v.z;
-          words[4 * c + 3] = v.w;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 o;
-          dequant_word8<AT>(words[2 * c], s2, b2, o.x, o.y);
-          dequant_word8<AT>(words[2 * c + 1], s2, b2, o.z, o.w);
-          *reinterpret_cast<uint4*>(arow + ((c ^ swz_a) << 4)) = o;
-        }
-      }
-      ptx::fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
-      __syncwarp();
-      if (lane == 0) {
-        ptx::mbar_arrive(afull_bar(s));
-        ptx::mbar_arrive(empty_bar(s));
-      }
-    }
-    }
-    // epilogue
-    if (ok) {
-      if (!ptx::mbar_wait(acc_bar, 0)) {
-        report(kStatusEpilogue);
-        ok = false;
-      }
-    }
-    if (ok) {
       ptx::tc_fence_after();
-      const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16);
+      const int n = (t % n_tiles) * kBM + r, m0 = (t / n_tiles) * BN;
+      const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(buf * BN);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t v[16];
         ptx::tmem_ld_32x32b_x16(t_lane + uint32_t(c0), v);
         ptx::tmem_wait_ld();
-        if (row_ok) {
+        if (n < N) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int m = m0 + c0 + j;
@@ -356,6 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(acce_bar + 8u * buf);
     }
   }
 
@@ -410,15 +456,16 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
                       void* y, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
   using L = Layout<BITS, BN>;
   constexpr int kMaxSmem = 227 * 1024;
-  const int stages = std::min(8, (kMaxSmem - 1024 - 256) / L::kStageBytes);
+  constexpr int kBarBytes = 512;
+  const int stages = std::min(8, (kMaxSmem - 1024 - kBarBytes) / L::kStageBytes);
   if (stages < 2) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: tile does not fit");
-  const size_t smem = size_t(stages) * L::kStageBytes + 1024 + 256;
+  const size_t smem = size_t(stages) * L::kStageBytes + 1024 + kBarBytes;
 
-  CUtensorMap tm_x, tm_w;
-  const CUtensorMapDataType xdt = std::is_same<AT, __half>::value
+  CUtensorMap tm_x, tm_w, tm_s, tm_b;
+  const CUtensorMapDataType adt = std::is_same<AT, __half>::value
                                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  qlin_status s = make_map(&tm_x, xdt, x, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, BN,
+  qlin_status s = make_map(&tm_x, adt, x, uint64_t(K), uint64_t(M), uint64_t(K) * 2, kBK, BN,
                            CU_TENSOR_MAP_SWIZZLE_128B);
   if (s != QLIN_OK) return s;
   const uint64_t wpr = uint64_t(K) * BITS / 32;
@@ -426,20 +473,36 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
                Geo<BITS>::kWordsPerGroup, kBM,
                BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (s != QLIN_OK) return s;
+  // scales/biases by TMA in boxes of 8 groups x 128 rows: needs 16-byte rows
+  const uint64_t gpr = uint64_t(K) / kGroup;
+  const bool scale_tma = gpr % 8 == 0 && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(biases) % 16 == 0;
+  if (scale_tma) {
+    if ((s = make_map(&tm_s, adt, scales, gpr, uint64_t(N), gpr * 2, 8, kBM,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) != QLIN_OK)
+      return s;
+    if ((s = make_map(&tm_b, adt, biases, gpr, uint64_t(N), gpr * 2, 8, kBM,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) != QLIN_OK)
+      return s;
+  } else {
+    tm_s = tm_x;  // unused
+    tm_b = tm_x;
+  }
 
-  auto kern = qmm_kernel<BITS, AT, BN>;
-  static int attr_dev = -1;
+  auto kern = scale_tma ? qmm_kernel<BITS, AT, BN, true> : qmm_kernel<BITS, AT, BN, false>;
+  static int attr_dev[2] = {-1, -1};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (attr_dev != dev) {
+  if (attr_dev[scale_tma] != dev) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
         cudaSuccess)
       return check_launch("qlin_qmm: cudaFuncSetAttribute");
-    attr_dev = dev;
+    attr_dev[scale_tma] = dev;
   }
-  const dim3 grid(unsigned((N + kBM - 1) / kBM), unsigned((M + BN - 1) / BN));
-  if (grid.y > 65535u) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: M too large");
-  kern<<<grid, kThreads, smem, st>>>(tm_x, tm_w, static_cast<const AT*>(scales),
+  const int64_t tiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
+  if (tiles > (int64_t(1) << 30)) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: too many tiles");
+  const int grid = int(std::min<int64_t>(tiles, sm_count()));  // persistent: one CTA per SM
+  kern<<<grid, kThreads, smem, st>>>(tm_x, tm_w, tm_s, tm_b, static_cast<const AT*>(scales),
                                      static_cast<const AT*>(biases), static_cast<AT*>(y), int(M),
                                      int(N), int(K), stages);
   return check_launch("qmm_kernel");
