@@ -12,18 +12,22 @@
 // the full 128-row MMA and large ones use BN = 128/256.
 //   D[n][m] (TMEM, f32) += W_hat[n][k] (smem, A operand) * x[m][k] (smem, B)
 //
-// Per CTA (one 128 x BN output tile, K loop in stages of one group = 64 k):
-//   warp 0      TMA producer: x tile [BN x 64] (128-byte swizzle) and the
-//               packed tile [128 rows x 64 codes] into stage s.
-//   warp 1      TMEM allocator and MMA issuer (one thread): 4 MMAs of K=16
-//               per stage, then tcgen05.commit to free the stage.
-//   warps 2..5  dequantisers (thread = weight row): unpack the row's 64 codes,
-//               w_hat = q*scale + bias in the operand type with one fused
-//               multiply-add (bit-identical to qlin_dequant's output), and
-//               store the 128-byte row into the A tile in the 128-byte swizzle
-//               layout the MMA descriptor expects.  After the K loop the same
-//               warps are the epilogue: tcgen05.ld of their TMEM lane quarter,
-//               RNE to the output type, coalesced stores along n.
+// Persistent CTAs (one per SM) walk 128 x BN output tiles; the K loop runs in
+// stages of one group (64 k) through a shared-memory ring:
+//   warp 0       TMA producer: x tile [BN x 64] (128-byte swizzle), packed
+//                tile [128 rows x 64 codes] (32/64-byte swizzle) and, when the
+//                scale rows are 16-byte aligned, the 8-group scale and bias
+//                boxes holding the stage's group.
+//   warp 1       TMEM allocator and MMA issuer (one thread): 4 MMAs of K=16
+//                per stage into one of two TMEM accumulators (tiles alternate),
+//                tcgen05.commit to free the stage / hand the tile over.
+//   warps 2..9   two dequantising warpgroups taking stages in turn (thread =
+//                weight row): unpack the row's 64 codes, w_hat = q*scale + bias
+//                in the operand type with one fused multiply-add (bit-identical
+//                to qlin_dequant's output), store the 128-byte row into the A
+//                tile in the 128-byte swizzle layout of the MMA descriptor.
+//   warps 10..13 epilogue: tcgen05.ld of their TMEM lane quarter, RNE to the
+//                output type, stores along n; overlaps the next tile's K loop.
 //
 // Every mbarrier wait is bounded (about 2 s); a wait that gives up records a
 // bit in a device status word, the CTA unwinds (waiting, bounded, for its own
@@ -47,7 +51,9 @@ namespace {
 
 constexpr int kBM = 128;          // weight rows per tile (MMA M)
 constexpr int kBK = 64;           // k per stage (one group)
-constexpr int kThreads = 14 * 32;  // TMA, MMA, 8 dequant, 4 epilogue warps
+constexpr int kDequantGroups = 2;   // warpgroups that dequantise stages in rotation
+constexpr int kDequantWarps = 4 * kDequantGroups;
+constexpr int kThreads = (2 + kDequantWarps + 4) * 32;  // TMA, MMA, dequant, 4 epilogue warps
 
 enum : unsigned {
   kStatusProducer = 1u,
@@ -173,10 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto w_addr = [&](int s) { return x_addr(s) + uint32_t(L::kWOff); };
   auto s_addr = [&](int s) { return x_addr(s) + uint32_t(L::kSOff); };
   const uint32_t bar_base = base + uint32_t(stages * L::kStageBytes);
-  auto full_bar = [&](int s) { return bar_base + 8u * s; };
-  auto empty_bar = [&](int s) { return bar_base + 8u * (stages + s); };
-  auto afull_bar = [&](int s) { return bar_base + 8u * (2 * stages + s); };
-  const uint32_t accf_bar = bar_base + 8u * (3 * stages);   // [2] MMA -> epilogue
+  // one "loaded" barrier per stage and dequantising group: use u of the ring
+  // (stage u % stages) signals the barrier of group u % kDequantGroups
+  auto full_bar = [&](int g, int s) { return bar_base + 8u * (g * stages + s); };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (kDequantGroups * stages + s); };
+  auto afull_bar = [&](int s) { return bar_base + 8u * ((kDequantGroups + 1) * stages + s); };
+  const uint32_t accf_bar = bar_base + 8u * ((kDequantGroups + 2) * stages);  // [2] MMA -> epilogue
   const uint32_t acce_bar = accf_bar + 16u;                   // [2] epilogue -> MMA
   const uint32_t done_bar = acce_bar + 16u;
   const uint32_t tmem_slot = done_bar + 8u;
@@ -184,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      ptx::mbar_init(full_bar(s), 1);
+      for (int g = 0; g < kDequantGroups; ++g) ptx::mbar_init(full_bar(g, s), 1);
       ptx::mbar_init(empty_bar(s), 1 + 4);  // MMA commit + the 4 warps of the dequant group
       ptx::mbar_init(afull_bar(s), 4);
     }
@@ -213,8 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int s = 0, issued = 0;
+      int s = 0, g = 0, issued = 0;
       uint32_t round = 0;
+      uint32_t full_ph = 0;  // bit g*8+s: parity of the next phase of full_bar(g, s)
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const int n0 = (t % n_tiles) * kBM, m0 = (t / n_tiles) * BN;
@@ -224,15 +233,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          ptx::mbar_arrive_expect_tx(full_bar(s), L::kTxBytes + (SCALE_TMA ? L::kSBytes : 0));
-          ptx::tma_load_2d(x_addr(s), &tm_x, full_bar(s), kb * kBK, m0);
-          ptx::tma_load_2d(w_addr(s), &tm_w, full_bar(s), kb * G::kWordsPerGroup, n0);
+          const uint32_t fb = full_bar(g, s);
+          ptx::mbar_arrive_expect_tx(fb, L::kTxBytes + (SCALE_TMA ? L::kSBytes : 0));
+          ptx::tma_load_2d(x_addr(s), &tm_x, fb, kb * kBK, m0);
+          ptx::tma_load_2d(w_addr(s), &tm_w, fb, kb * G::kWordsPerGroup, n0);
           if constexpr (SCALE_TMA) {
             // the 8 groups holding group kb (x coordinate a multiple of 8 groups = 16 bytes)
-            ptx::tma_load_2d(s_addr(s), &tm_s, full_bar(s), kb & ~7, n0);
-            ptx::tma_load_2d(s_addr(s) + uint32_t(kBM * 16), &tm_b, full_bar(s), kb & ~7, n0);
+            ptx::tma_load_2d(s_addr(s), &tm_s, fb, kb & ~7, n0);
+            ptx::tma_load_2d(s_addr(s) + uint32_t(kBM * 16), &tm_b, fb, kb & ~7, n0);
           }
+          full_ph ^= 1u << (g * 8 + s);
           ++issued;
+          if (++g == kDequantGroups) g = 0;
           if (++s == stages) {
             s = 0;
             ++round;
@@ -240,10 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) {
+        // the last min(issued, stages) loads, one per stage, may be in flight:
+        // wait (bounded) for each before the CTA exits
         const int first = issued > stages ? issued - stages : 0;
-        for (int v = first; v < issued; ++v)
-          if (!ptx::mbar_wait(full_bar(v % stages), uint32_t(v / stages) & 1u))
-            report(kStatusTeardown);
+        for (int v = first; v < issued; ++v) {
+          const int vg = v % kDequantGroups, vs = v % stages;
+          const uint32_t parity = ((full_ph >> (vg * 8 + vs)) & 1u) ^ 1u;
+          if (!ptx::mbar_wait(full_bar(vg, vs), parity)) report(kStatusTeardown);
+        }
       }
     }
   } else if (warp == 1) {
@@ -251,8 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t fmt = std::is_same<AT, __half>::value ? 0u : 1u;
       constexpr uint32_t idesc = ptx::idesc_f16(fmt, kBM, BN);
-      int s = 0, i = 0;
+      int s = 0, g = 0, i = 0;
       uint32_t round = 0;
+      uint32_t full_ph = 0;  // bit g*8+s: parity of the next phase of full_bar(g, s)
       bool ok = true, any = false;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++i) {
         const int buf = i & 1;
@@ -264,7 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
         for (int kb = 0; kb < kb_count; ++kb) {
-          if (!ptx::mbar_wait(afull_bar(s), round & 1u) || !ptx::mbar_wait(full_bar(s), round & 1u)) {
+          if (!ptx::mbar_wait(afull_bar(s), round & 1u) ||
+              !ptx::mbar_wait(full_bar(g, s), (full_ph >> (g * 8 + s)) & 1u)) {
             report(kStatusMma);
             ok = false;
             break;
@@ -280,6 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           any = true;
           ptx::mma_commit(empty_bar(s));
+          full_ph ^= 1u << (g * 8 + s);
+          if (++g == kDequantGroups) g = 0;
           if (++s == stages) {
             s = 0;
             ++round;
@@ -291,15 +311,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mma_commit(done_bar);
       if (any && !ptx::mbar_wait(done_bar, 0)) report(kStatusTeardown);
     }
-  } else if (warp < 2 + 8) {
-    // -------------------------------------------- dequantise (two groups)
-    const int grp = (warp - 2) >> 2;  // stages with (use index & 1) == grp
+  } else if (warp < 2 + kDequantWarps) {
+    // -------------------------------- dequantise (warpgroups take uses in turn)
+    // Group g takes the ring uses u with u % kDequantGroups == g and waits on
+    // its own barriers full_bar(g, .), whose phases it alone consumes, in
+    // order: it can never wait on a phase two ahead of a barrier's last
+    // completed one (a parity wait cannot tell those apart), whatever the ring
+    // depth.
+    const int grp = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // weight row within the tile
     const int gpr = K / kGroup;
     const int swz_a = r & 7;
     int s = 0, u = 0;
-    uint32_t round = 0;
+    uint32_t full_ph = 0;  // bit s: parity of the next phase of full_bar(grp, s)
     bool ok = true;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const int n = (t % n_tiles) * kBM + r;
@@ -308,22 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const AT* brow = biases + int64_t(min(n, N - 1)) * gpr;
       for (int kb = 0; kb < kb_count; ++kb, ++u) {
         const int cs = s;
-        const uint32_t cround = round;
-        if (++s == stages) {
-          s = 0;
-          ++round;
-        }
-        if ((u & 1) != grp) continue;
+        if (++s == stages) s = 0;
+        if (u % kDequantGroups != grp) continue;
         AT sc, bc;
         if constexpr (!SCALE_TMA) {
           sc = srow[kb];
           bc = brow[kb];
         }
-        if (!ptx::mbar_wait(full_bar(cs), cround & 1u)) {
+        if (!ptx::mbar_wait(full_bar(grp, cs), (full_ph >> cs) & 1u)) {
           report(kStatusDequant);
           ok = false;
           break;
         }
+        full_ph ^= 1u << cs;
         if constexpr (SCALE_TMA) {
           const AT* ss = reinterpret_cast<const AT*>(gbase + (s_addr(cs) - base));
           sc = ss[r * 8 + (kb & 7)];
@@ -457,6 +479,9 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
   using L = Layout<BITS, BN>;
   constexpr int kMaxSmem = 227 * 1024;
   constexpr int kBarBytes = 512;
+  // (kDequantGroups + 2) barriers per stage (at most 8), two pairs of
+  // accumulator barriers, the teardown barrier and the TMEM address slot
+  static_assert((kDequantGroups + 2) * 8 * 8 + 4 * 8 + 8 + 4 <= kBarBytes, "barrier block");
   const int stages = std::min(8, (kMaxSmem - 1024 - kBarBytes) / L::kStageBytes);
   if (stages < 2) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: tile does not fit");
   const size_t smem = size_t(stages) * L::kStageBytes + 1024 + kBarBytes;

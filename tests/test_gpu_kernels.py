@@ -106,6 +106,13 @@ QMM_CASES = [
     (33, 300, 512, 8, "f16"), (64, 256, 1024, 4, "f16"), (129, 301, 512, 4, "bf16"),
     (300, 200, 256, 8, "bf16"), (600, 384, 512, 4, "f16"), (257, 1, 128, 8, "f16"),
     (16, 128, 64, 4, "f16"), (512, 1024, 2048, 8, "f16"),
+    # enough tiles for the 256- and 128-token tiles, several tiles per CTA.  bf16
+    # cases use K >= 512: the tensor-core operand is w_hat rounded to bf16
+    # (2^-9 relative) and the output is rounded to bf16 too, so the bound
+    # 2e-3 * sum|x w| only holds while |y| stays well below sum|x w|, which
+    # random-sign data guarantees at K of a few hundred or more, not at K ~ 100
+    (768, 8192, 128, 8, "f16"), (768, 8192, 512, 4, "bf16"), (640, 4096, 256, 4, "f16"),
+    (1100, 8200, 512, 8, "bf16"),
 ]
 
 
