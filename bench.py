@@ -72,11 +72,24 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def profile_traffic(profile_name: str, source_file: str):
+# sources of qmv_kernel: a recorded traffic figure is used only while they are
+# byte-identical to the ones the capture was taken with
+QMV_SOURCES = ("qmv.cu", "qmv_core.cuh", "device_common.cuh", "sm100_ptx.cuh")
+
+
+def sources_sha256(sources) -> str:
+    """SHA-256 over the named kernel sources, concatenated in order."""
+    h = hashlib.sha256()
+    for name in sources:
+        with open(os.path.join(ROOT, "int8_qmv_qmm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profile_traffic(profile_name: str, sources):
     """DRAM bytes per launch recorded by an ncu capture under profiles/, or
-    None when absent or when the kernel source changed since the capture."""
+    None when absent or when the kernel's sources changed since the capture."""
     prof = os.path.join(ROOT, "profiles", profile_name)
-    src = os.path.join(ROOT, "int8_qmv_qmm_gb300", "csrc", source_file)
     try:
         fields = {}
         with open(prof) as f:
@@ -85,9 +98,7 @@ def profile_traffic(profile_name: str, source_file: str):
                                                             "source_sha256")):
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
-        with open(src, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
-        if fields.get("source_sha256") != sha:
+        if fields.get("source_sha256") != sources_sha256(sources):
             return None
         return float(fields["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -508,7 +519,7 @@ def bench_ours(args):
     cpu = None if args.no_cpu_baseline else run_oracle_baseline()
     clocks = sampler.summary()
     bytes_step = step.packed_bytes()
-    traffic = profile_traffic("qmv_decode_step.txt", "qmv.cu")
+    traffic = profile_traffic("qmv_decode_step.txt", QMV_SOURCES)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
