@@ -3,31 +3,38 @@
 //
 // y[m][n] = sum_k x[m][k] * w_hat[n][k],  w_hat = q*scale + bias (per group of 64)
 //
-// The reconstructed weight only ever exists as a shared-memory operand tile:
-// it is never written to DRAM ("track(upstream-iree): fused dequant->matmul
-// for the packed int8 bandwidth win", section "The blocker (measured)").
+// The reconstructed weight only ever exists in tensor memory, as the MMA's A
+// operand: it is never written to DRAM, nor to shared memory ("track(upstream-
+// iree): fused dequant->matmul for the packed int8 bandwidth win", section
+// "The blocker (measured)").
 //
 // Orientation ("swap AB"): the MMA's M dimension is 128 weight rows and its N
 // dimension is a tile of BN tokens, so small batches (BN = 16..64) still use
 // the full 128-row MMA and large ones use BN = 128/256.
-//   D[n][m] (TMEM, f32) += W_hat[n][k] (smem, A operand) * x[m][k] (smem, B)
+//   D[n][m] (TMEM, f32) += W_hat[n][k] (TMEM, A operand) * x[m][k] (smem, B)
 //
 // Persistent CTAs (one per SM) walk 128 x BN output tiles; the K loop runs in
-// stages of one group (64 k) through a shared-memory ring:
+// stages of one group (64 k) through a ring of shared-memory stages and, with
+// the same index, of TMEM A slots:
 //   warp 0       TMA producer: x tile [BN x 64] (128-byte swizzle), packed
 //                tile [128 rows x 64 codes] (32/64-byte swizzle) and, when the
 //                scale rows are 16-byte aligned, the 8-group scale and bias
 //                boxes holding the stage's group.
 //   warp 1       TMEM allocator and MMA issuer (one thread): 4 MMAs of K=16
-//                per stage into one of two TMEM accumulators (tiles alternate),
-//                tcgen05.commit to free the stage / hand the tile over.
+//                per stage (A from the stage's TMEM slot, B = x from shared
+//                memory) into a TMEM accumulator (two, alternating by tile,
+//                when BN <= 128), tcgen05.commit to free the stage / hand the
+//                tile over.
 //   warps 2..9   two dequantising warpgroups taking stages in turn (thread =
-//                weight row): unpack the row's 64 codes, w_hat = q*scale + bias
-//                in the operand type with one fused multiply-add (bit-identical
-//                to qlin_dequant's output), store the 128-byte row into the A
-//                tile in the 128-byte swizzle layout of the MMA descriptor.
+//                weight row = TMEM lane): unpack the row's 64 codes, w_hat =
+//                q*scale + bias in the operand type with one fused
+//                multiply-add (bit-identical to qlin_dequant's output), and
+//                write the row into the stage's A slot with one tcgen05.st.
+//                Keeping A out of shared memory leaves its bandwidth to the
+//                TMA writes and the MMA's reads of x.
 //   warps 10..13 epilogue: tcgen05.ld of their TMEM lane quarter, RNE to the
-//                output type, stores along n; overlaps the next tile's K loop.
+//                output type, stores along n; with two accumulators it
+//                overlaps the next tile's K loop.
 //
 // Every mbarrier wait is bounded (about 2 s); a wait that gives up records a
 // bit in a device status word, the CTA unwinds (waiting, bounded, for its own
@@ -65,6 +72,40 @@ enum : unsigned {
 
 __device__ __forceinline__ void report(unsigned bit) { atomicOr(&g_qmm_status, bit); }
 
+// D (TMEM, f32) += A (TMEM: row i in lane i, K along columns, two 16-bit
+// elements per 32-bit column, element k in the low half) * B (shared memory
+// descriptor); M = 128, accumulate = 0 overwrites D.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Each thread of the warp writes 32 consecutive 32-bit columns of its own TMEM
+// lane (lane = the warp's lane quarter * 32 + lane id, taken from taddr).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Wait until this thread's tcgen05.st have completed.
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+
 template <int BITS>
 struct Geo {
   static constexpr int kWordsPerGroup = kBK * BITS / 32;           // 8 or 16
@@ -74,18 +115,24 @@ struct Geo {
 
 __host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
+// Shared-memory stage: [x tile][packed tile][8 groups of scales, of biases].
+// TMEM: kDBufs accumulators of BN columns, then one 32-column slot per ring
+// stage holding the stage's dequantised A tile (128 lanes x 64 16-bit values).
 template <int BITS, int BN>
 struct Layout {
   static constexpr int kXBytes = BN * kBK * 2;           // x tile, 128-byte rows
-  static constexpr int kABytes = kBM * kBK * 2;          // dequantised tile
   static constexpr int kWBytes = Geo<BITS>::kPackedBytes;
   static constexpr int kSBytes = 2 * kBM * 16;           // 8 groups of scales + of biases
-  static constexpr int kXOff = round_up(kXBytes, 1024);
-  static constexpr int kWOff = kXOff + kABytes;
+  static constexpr int kWOff = round_up(kXBytes, 1024);
   static constexpr int kSOff = kWOff + round_up(kWBytes, 1024);
   static constexpr int kStageBytes = kSOff + round_up(kSBytes, 1024);
   static constexpr int kTxBytes = kXBytes + kWBytes;
-  static constexpr uint32_t kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+  // two accumulators (the epilogue of a tile overlaps the next tile's K loop)
+  // unless they would leave TMEM too few A slots
+  static constexpr int kDBufs = BN >= 256 ? 1 : 2;
+  static constexpr int kACol0 = kDBufs * BN < 32 ? 32 : kDBufs * BN;
+  static constexpr int kAColsPerStage = kBK / 2;         // 64 16-bit values per lane
+  static constexpr int kMaxStages = (512 - kACol0) / kAColsPerStage;
 };
 
 // ---- unpack + dequantise one 16-bit pair: returns (w_hat[2j], w_hat[2j+1])
@@ -160,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
                const AT* __restrict__ scales, const AT* __restrict__ biases, AT* __restrict__ y,
-               int M, int N, int K, int stages) {
+               int M, int N, int K, int stages, int tmem_cols) {
   using L = Layout<BITS, BN>;
   using G = Geo<BITS>;
   extern __shared__ uint8_t smem_raw[];
@@ -173,9 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (N + kBM - 1) / kBM, m_tiles = (M + BN - 1) / BN;
   const int total_tiles = n_tiles * m_tiles;
 
-  // stage s: [x tile][A tile][packed tile][scales][biases]
+  // stage s: [x tile][packed tile][scales][biases]
   auto x_addr = [&](int s) { return base + uint32_t(s * L::kStageBytes); };
-  auto a_addr = [&](int s) { return x_addr(s) + uint32_t(L::kXOff); };
   auto w_addr = [&](int s) { return x_addr(s) + uint32_t(L::kWOff); };
   auto s_addr = [&](int s) { return x_addr(s) + uint32_t(L::kSOff); };
   const uint32_t bar_base = base + uint32_t(stages * L::kStageBytes);
@@ -210,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, L::kTmemCols);
+    ptx::tmem_alloc(tmem_slot, uint32_t(tmem_cols));
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -272,8 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t full_ph = 0;  // bit g*8+s: parity of the next phase of full_bar(g, s)
       bool ok = true, any = false;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++i) {
-        const int buf = i & 1;
-        if (i >= 2 && !ptx::mbar_wait(acce_bar + 8u * buf, uint32_t((i >> 1) - 1) & 1u)) {
+        const int buf = i % L::kDBufs;
+        if (i >= L::kDBufs &&
+            !ptx::mbar_wait(acce_bar + 8u * buf, uint32_t(i / L::kDBufs - 1) & 1u)) {
           report(kStatusMma);
           ok = false;
           break;
@@ -288,13 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint64_t ad = ptx::sw128_kmajor_desc(a_addr(s));
+          const uint32_t a_tmem =
+              tmem_base + uint32_t(L::kACol0 + s * L::kAColsPerStage);
           const uint64_t bd = ptx::sw128_kmajor_desc(x_addr(s));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            // +32 bytes along K = +2 in the descriptor's 16-byte address units
-            ptx::mma_f16_ss(d_tmem, ad + uint64_t(2 * kk), bd + uint64_t(2 * kk), idesc,
-                            (kb > 0 || kk > 0) ? 1u : 0u);
+            // K = 16 per MMA: 8 TMEM columns of A; +32 bytes of the x rows =
+            // +2 in the descriptor's 16-byte address units
+            mma_f16_ts(d_tmem, a_tmem + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc,
+                       (kb > 0 || kk > 0) ? 1u : 0u);
           }
           any = true;
           ptx::mma_commit(empty_bar(s));
@@ -322,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // weight row within the tile
     const int gpr = K / kGroup;
-    const int swz_a = r & 7;
+    // this thread's TMEM lane (its weight row) at the first A slot
+    const uint32_t a_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(L::kACol0);
     int s = 0, u = 0;
     uint32_t full_ph = 0;  // bit s: parity of the next phase of full_bar(grp, s)
     bool ok = true;
@@ -340,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           sc = srow[kb];
           bc = brow[kb];
         }
-        if (!ptx::mbar_wait(full_bar(grp, cs), (full_ph >> cs) & 1u)) {
+        // warp-uniform outcome: tcgen05.st below needs the whole warp
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait(full_bar(grp, cs), (full_ph >> cs) & 1u))) {
           report(kStatusDequant);
           ok = false;
           break;
@@ -353,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t s2 = row_ok ? splat(sc) : 0u, b2 = row_ok ? splat(bc) : 0u;
         const uint8_t* wrow = gbase + (w_addr(cs) - base) + r * G::kPackedRowBytes;
-        uint8_t* arow = gbase + (a_addr(cs) - base) + r * 128;
+        // the row's 64 reconstructed weights, two per register, k ascending
+        uint32_t a[32];
         if constexpr (BITS == 4) {
           // packed rows are 32 bytes in the 32-byte TMA swizzle: chunk c of row
           // r sits at chunk c ^ ((r >> 2) & 1)
@@ -362,9 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 hi = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
           const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(arow + ((c ^ swz_a) << 4)) =
-                dequant_word4<AT>(words[c], s2, b2);
+          for (int c = 0; c < 8; ++c) {
+            const uint4 o = dequant_word4<AT>(words[c], s2, b2);
+            a[4 * c] = o.x;
+            a[4 * c + 1] = o.y;
+            a[4 * c + 2] = o.z;
+            a[4 * c + 3] = o.w;
+          }
         } else {
           // packed rows are 64 bytes in the 64-byte TMA swizzle: chunk c of row
           // r sits at chunk c ^ ((r >> 1) & 3)
@@ -380,13 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            uint4 o;
-            dequant_word8<AT>(words[2 * c], s2, b2, o.x, o.y);
-            dequant_word8<AT>(words[2 * c + 1], s2, b2, o.z, o.w);
-            *reinterpret_cast<uint4*>(arow + ((c ^ swz_a) << 4)) = o;
+            dequant_word8<AT>(words[2 * c], s2, b2, a[4 * c], a[4 * c + 1]);
+            dequant_word8<AT>(words[2 * c + 1], s2, b2, a[4 * c + 2], a[4 * c + 3]);
           }
         }
-        ptx::fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
+        // into the stage's A slot; complete before the MMA issuer is told
+        tmem_st_32x32b_x32(a_lane + uint32_t(cs * L::kAColsPerStage), a);
+        tmem_wait_st();
+        ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           ptx::mbar_arrive(afull_bar(cs));
@@ -400,30 +457,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     int i = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
-      const int buf = i & 1;
-      if (!ptx::mbar_wait(accf_bar + 8u * buf, uint32_t(i >> 1) & 1u)) {
+      const int buf = i % L::kDBufs;
+      if (!__all_sync(0xffffffffu,
+                      ptx::mbar_wait(accf_bar + 8u * buf, uint32_t(i / L::kDBufs) & 1u))) {
         report(kStatusEpilogue);
         break;
       }
       ptx::tc_fence_after();
       const int n = (t % n_tiles) * kBM + r, m0 = (t / n_tiles) * BN;
       const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(buf * BN);
+      // batches of up to 64 columns: four loads, one wait (a TMEM load's
+      // latency per batch, not per 16 columns); the accumulator is handed
+      // back to the MMA issuer as soon as the last batch is in registers
+      constexpr int kBatch = BN < 64 ? BN : 64;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t v[16];
-        ptx::tmem_ld_32x32b_x16(t_lane + uint32_t(c0), v);
+      for (int c0 = 0; c0 < BN; c0 += kBatch) {
+        uint32_t v[kBatch];
+#pragma unroll
+        for (int c = 0; c < kBatch; c += 16)
+          ptx::tmem_ld_32x32b_x16(t_lane + uint32_t(c0 + c),
+                                  *reinterpret_cast<uint32_t(*)[16]>(v + c));
         ptx::tmem_wait_ld();
+        if (c0 + kBatch >= BN) {
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(acce_bar + 8u * buf);
+        }
         if (n < N) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < kBatch; ++j) {
             const int m = m0 + c0 + j;
             if (m < M) y[int64_t(m) * N + n] = Act<AT>::from_f32_rn(__uint_as_float(v[j]));
           }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(acce_bar + 8u * buf);
     }
   }
 
@@ -432,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, L::kTmemCols);
+    ptx::tmem_dealloc(tmem_base, uint32_t(tmem_cols));
   }
 }
 
@@ -482,9 +549,15 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
   // (kDequantGroups + 2) barriers per stage (at most 8), two pairs of
   // accumulator barriers, the teardown barrier and the TMEM address slot
   static_assert((kDequantGroups + 2) * 8 * 8 + 4 * 8 + 8 + 4 <= kBarBytes, "barrier block");
-  const int stages = std::min(8, (kMaxSmem - 1024 - kBarBytes) / L::kStageBytes);
+  const int stages =
+      std::min(std::min(8, L::kMaxStages), (kMaxSmem - 1024 - kBarBytes) / L::kStageBytes);
   if (stages < 2) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: tile does not fit");
   const size_t smem = size_t(stages) * L::kStageBytes + 1024 + kBarBytes;
+  // TMEM columns: the accumulators and one A slot per stage, rounded up to a
+  // power of two (tcgen05.alloc); at most 512
+  int tmem_cols = 32;
+  while (tmem_cols < L::kACol0 + stages * L::kAColsPerStage) tmem_cols *= 2;
+  if (tmem_cols > 512) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: TMEM layout does not fit");
 
   CUtensorMap tm_x, tm_w, tm_s, tm_b;
   const CUtensorMapDataType adt = std::is_same<AT, __half>::value
@@ -529,7 +602,7 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
   const int grid = int(std::min<int64_t>(tiles, sm_count()));  // persistent: one CTA per SM
   kern<<<grid, kThreads, smem, st>>>(tm_x, tm_w, tm_s, tm_b, static_cast<const AT*>(scales),
                                      static_cast<const AT*>(biases), static_cast<AT*>(y), int(M),
-                                     int(N), int(K), stages);
+                                     int(N), int(K), stages, tmem_cols);
   return check_launch("qmm_kernel");
 }
 
