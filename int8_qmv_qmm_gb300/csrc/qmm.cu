@@ -43,6 +43,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 #include <type_traits>
 
@@ -609,13 +610,33 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
 template <int BITS, typename AT>
 qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
-  // Token tile: the whole batch when it is small; otherwise the largest tile
-  // that still gives every SM a CTA.
-  int bn = 16;
-  while (bn < 256 && bn < M) bn <<= 1;
+  // Token tile: pick the BN with the smallest estimated time, waves of
+  // persistent tiles x stages per tile x time per stage.  A stage's time is
+  // set by the 128 x BN x 64 MMA for large BN and by a fixed floor (the TMA
+  // requests and the dequantisation of the 128 x 64 weight tile, the same for
+  // every BN) for small BN; measured on GB300 as about 0.40 us at BN = 256
+  // and 0.27-0.30 us at BN <= 128.  Ties go to the larger tile.
+  int max_bn = 16;
+  while (max_bn < 256 && max_bn < M) max_bn <<= 1;
   const int64_t sms = sm_count();
   const int64_t n_tiles = (N + kBM - 1) / kBM;
-  while (bn > 64 && n_tiles * ((M + bn - 1) / bn) < sms) bn >>= 1;
+  int bn = max_bn;
+  double best = -1.0;
+  for (int cand = max_bn; cand >= 16; cand >>= 1) {
+    const int64_t tiles = n_tiles * ((M + cand - 1) / cand);
+    const int64_t waves = (tiles + sms - 1) / sms;
+    const double t_stage = std::max(0.27, 0.40 * cand / 256.0);
+    const double cost = double(waves) * t_stage;
+    if (best < 0.0 || cost < best * 0.97) {
+      best = cost;
+      bn = cand;
+    }
+  }
+  // QLIN_QMM_BN (16, 32, 64, 128 or 256) overrides the choice, for tuning
+  if (const char* env = std::getenv("QLIN_QMM_BN")) {
+    const int v = std::atoi(env);
+    if (v == 16 || v == 32 || v == 64 || v == 128 || v == 256) bn = v;
+  }
   switch (bn) {
     case 16: return launch_bn<BITS, AT, 16>(x, wq, scales, biases, y, M, N, K, st);
     case 32: return launch_bn<BITS, AT, 32>(x, wq, scales, biases, y, M, N, K, st);
