@@ -197,6 +197,40 @@ __device__ __forceinline__ void dequant_word8<__nv_bfloat16>(uint32_t w, uint32_
   p1 = *reinterpret_cast<const uint32_t*>(&r1);
 }
 
+// ---- thread-block cluster helpers (split-K reduction)
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster; release/acquire orders the
+// shared::cluster stores made before it with the loads made after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The address of this CTA's shared-memory location `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory; its bytes are
+// counted (complete_tx) on that CTA's mbarrier `bar` (a shared::cluster
+// address too).
+__device__ __forceinline__ void st_async_f32x4(uint32_t addr, float a, float b, float c, float d,
+                                               uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+      : "memory");
+}
+
 template <typename AT>
 __device__ __forceinline__ uint32_t splat(AT v) {
   const uint16_t u = *reinterpret_cast<const uint16_t*>(&v);
@@ -208,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
                const AT* __restrict__ scales, const AT* __restrict__ biases, AT* __restrict__ y,
-               int M, int N, int K, int stages, int tmem_cols) {
+               int M, int N, int K, int stages, int tmem_cols, int split) {
   using L = Layout<BITS, BN>;
   using G = Geo<BITS>;
   extern __shared__ uint8_t smem_raw[];
@@ -220,6 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb_count = K / kBK;
   const int n_tiles = (N + kBM - 1) / kBM, m_tiles = (M + BN - 1) / BN;
   const int total_tiles = n_tiles * m_tiles;
+  // split == 1: persistent CTAs walk tiles blockIdx.x, + gridDim.x, ...
+  // split  > 1: a cluster of `split` CTAs shares one tile (grid = tiles x
+  // split), CTA `rank` taking k-blocks [kb0, kb1); the partial accumulators
+  // are summed through distributed shared memory at the end.
+  const int rank = split > 1 ? int(cluster_ctarank()) : 0;
+  const int t_first = int(blockIdx.x) / split, t_step = int(gridDim.x) / split;
+  const int kb0 = rank * kb_count / split, kb1 = (rank + 1) * kb_count / split;
 
   // stage s: [x tile][packed tile][scales][biases]
   auto x_addr = [&](int s) { return base + uint32_t(s * L::kStageBytes); };
@@ -234,7 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t accf_bar = bar_base + 8u * ((kDequantGroups + 2) * stages);  // [2] MMA -> epilogue
   const uint32_t acce_bar = accf_bar + 16u;                   // [2] epilogue -> MMA
   const uint32_t done_bar = acce_bar + 16u;
-  const uint32_t tmem_slot = done_bar + 8u;
+  const uint32_t red_bar = done_bar + 8u;  // split-K: partials received
+  const uint32_t tmem_slot = red_bar + 8u;
   uint32_t* tmem_slot_ptr = reinterpret_cast<uint32_t*>(gbase + (tmem_slot - base));
 
   if (threadIdx.x == 0) {
@@ -248,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(acce_bar + 8u * b, 4);  // the epilogue warps
     }
     ptx::mbar_init(done_bar, 1);
+    ptx::mbar_init(red_bar, 1);
     ptx::fence_mbar_init();
     ptx::tma_prefetch_desc(&tm_x);
     ptx::tma_prefetch_desc(&tm_w);
@@ -272,9 +315,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t round = 0;
       uint32_t full_ph = 0;  // bit g*8+s: parity of the next phase of full_bar(g, s)
       bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      for (int t = t_first; t < total_tiles && ok; t += t_step) {
         const int n0 = (t % n_tiles) * kBM, m0 = (t / n_tiles) * BN;
-        for (int kb = 0; kb < kb_count; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (round > 0 && !ptx::mbar_wait(empty_bar(s), (round - 1) & 1u)) {
             report(kStatusProducer);
             ok = false;
@@ -318,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t round = 0;
       uint32_t full_ph = 0;  // bit g*8+s: parity of the next phase of full_bar(g, s)
       bool ok = true, any = false;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++i) {
+      for (int t = t_first; t < total_tiles && ok; t += t_step, ++i) {
         const int buf = i % L::kDBufs;
         if (i >= L::kDBufs &&
             !ptx::mbar_wait(acce_bar + 8u * buf, uint32_t(i / L::kDBufs - 1) & 1u)) {
@@ -328,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
-        for (int kb = 0; kb < kb_count; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!ptx::mbar_wait(afull_bar(s), round & 1u) ||
               !ptx::mbar_wait(full_bar(g, s), (full_ph >> (g * 8 + s)) & 1u)) {
             report(kStatusMma);
@@ -344,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // K = 16 per MMA: 8 TMEM columns of A; +32 bytes of the x rows =
             // +2 in the descriptor's 16-byte address units
             mma_f16_ts(d_tmem, a_tmem + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc,
-                       (kb > 0 || kk > 0) ? 1u : 0u);
+                       (kb > kb0 || kk > 0) ? 1u : 0u);
           }
           any = true;
           ptx::mma_commit(empty_bar(s));
@@ -377,12 +420,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s = 0, u = 0;
     uint32_t full_ph = 0;  // bit s: parity of the next phase of full_bar(grp, s)
     bool ok = true;
-    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+    for (int t = t_first; t < total_tiles && ok; t += t_step) {
       const int n = (t % n_tiles) * kBM + r;
       const bool row_ok = n < N;
       const AT* srow = scales + int64_t(min(n, N - 1)) * gpr;
       const AT* brow = biases + int64_t(min(n, N - 1)) * gpr;
-      for (int kb = 0; kb < kb_count; ++kb, ++u) {
+      for (int kb = kb0; kb < kb1; ++kb, ++u) {
         const int cs = s;
         if (++s == stages) s = 0;
         if (u % kDequantGroups != grp) continue;
@@ -457,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;
     int i = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
+    for (int t = t_first; t < total_tiles; t += t_step, ++i) {
       const int buf = i % L::kDBufs;
       if (!__all_sync(0xffffffffu,
                       ptx::mbar_wait(accf_bar + 8u * buf, uint32_t(i / L::kDBufs) & 1u))) {
@@ -465,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
+      if (split > 1) break;  // partial accumulator: reduced across the cluster below
       const int n = (t % n_tiles) * kBM + r, m0 = (t / n_tiles) * BN;
       const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(buf * BN);
       // batches of up to 64 columns: four loads, one wait (a TMEM load's
@@ -497,6 +541,124 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+
+  if (split > 1) {
+    // ---------------------------------------------- split-K reduction
+    // The tile's BN columns are cut into `split` slices; CTA d owns slice d.
+    // Every CTA sends its partial of each other slice d to CTA d's shared
+    // memory (the ring, idle once every CTA of the cluster is past its K
+    // loop): receive buffer [split-1 sources][slice/4][128 rows] of float4,
+    // row-minor so that a warp's 16-byte stores fall in distinct banks.
+    // Each owner then adds the partials in a fixed order (its own first,
+    // then the sources by rank) and stores its slice.
+    const bool epi = warp >= 2 + kDequantWarps && t_first < total_tiles;
+    const int slice = BN / split;
+    // arm the receive barrier with every byte the other CTAs will send
+    // before any of them can start (the cluster barrier below)
+    if (threadIdx.x == 0 && t_first < total_tiles)
+      ptx::mbar_arrive_expect_tx(red_bar, uint32_t((split - 1) * slice * kBM * 4));
+    cluster_sync();  // every CTA of the cluster is past its K loop and armed
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16);
+    // batches of up to 64 columns: four TMEM loads, one wait
+    constexpr int kRBatch = BN < 64 ? BN : 64;
+    const int batch = slice < kRBatch ? slice : kRBatch;
+    if (epi) {
+      for (int d = 0; d < split; ++d) {
+        if (d == rank) continue;
+        const int slot = rank < d ? rank : rank - 1;
+        const uint32_t dst =
+            map_shared_rank(base, uint32_t(d)) + uint32_t(slot * (slice / 4) * kBM * 16);
+        const uint32_t dst_bar = map_shared_rank(red_bar, uint32_t(d));
+#pragma unroll 1
+        for (int c0 = 0; c0 < slice; c0 += batch) {
+          uint32_t v[kRBatch];
+#pragma unroll
+          for (int c = 0; c < kRBatch; c += 16)
+            if (c < batch)
+              ptx::tmem_ld_32x32b_x16(t_lane + uint32_t(d * slice + c0 + c),
+                                      *reinterpret_cast<uint32_t(*)[16]>(v + c));
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < kRBatch / 4; ++q)
+            if (q < batch / 4)
+              st_async_f32x4(dst + uint32_t(((c0 / 4 + q) * kBM + r) * 16),
+                             __uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]),
+                             dst_bar);
+        }
+      }
+    }
+    // every partial destined to this CTA has landed (bounded wait)
+    const bool got = !epi || __all_sync(0xffffffffu, ptx::mbar_wait(red_bar, 0));
+    if (!got) report(kStatusEpilogue);
+    // (the block runs whether or not the wait succeeded: its named barrier
+    // needs all four epilogue warps; a timeout is reported, the values are
+    // then garbage)
+    if (epi) {
+      // sum into f16/bf16, stage [slice tokens][128 rows] in shared memory
+      // (after the receive buffer), then store y with 16-byte vectors
+      const int t = t_first;
+      const int n0 = (t % n_tiles) * kBM, m0 = (t / n_tiles) * BN + rank * slice;
+      AT* stage_y = reinterpret_cast<AT*>(gbase + (split - 1) * slice * kBM * 4);
+#pragma unroll 1
+      for (int c0 = 0; c0 < slice; c0 += batch) {
+        uint32_t v[kRBatch];
+#pragma unroll
+        for (int c = 0; c < kRBatch; c += 16)
+          if (c < batch)
+            ptx::tmem_ld_32x32b_x16(t_lane + uint32_t(rank * slice + c0 + c),
+                                    *reinterpret_cast<uint32_t(*)[16]>(v + c));
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < kRBatch / 4; ++q) {
+          if (q < batch / 4) {
+            float a0 = __uint_as_float(v[4 * q]), a1 = __uint_as_float(v[4 * q + 1]);
+            float a2 = __uint_as_float(v[4 * q + 2]), a3 = __uint_as_float(v[4 * q + 3]);
+            for (int src = 0; src < split - 1; ++src) {
+              const float4 p = *reinterpret_cast<const float4*>(
+                  gbase + ((src * (slice / 4) + c0 / 4 + q) * kBM + r) * 16);
+              a0 += p.x;
+              a1 += p.y;
+              a2 += p.z;
+              a3 += p.w;
+            }
+            const int mm = c0 + 4 * q;
+            stage_y[(mm + 0) * kBM + r] = Act<AT>::from_f32_rn(a0);
+            stage_y[(mm + 1) * kBM + r] = Act<AT>::from_f32_rn(a1);
+            stage_y[(mm + 2) * kBM + r] = Act<AT>::from_f32_rn(a2);
+            stage_y[(mm + 3) * kBM + r] = Act<AT>::from_f32_rn(a3);
+          }
+        }
+      }
+      // the four epilogue warps' rows are all staged
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+      const int et = threadIdx.x - (2 + kDequantWarps) * 32;  // 0..127
+      const bool vec = N % 8 == 0 && n0 + kBM <= N &&
+                       reinterpret_cast<uintptr_t>(y) % 16 == 0;
+      if (vec) {
+        // 16 chunks of 8 rows per token
+#pragma unroll 1
+        for (int c = et; c < slice * 16; c += 128) {
+          const int mm = c >> 4, n8 = (c & 15) * 8;
+          if (m0 + mm < M)
+            *reinterpret_cast<uint4*>(y + int64_t(m0 + mm) * N + n0 + n8) =
+                *reinterpret_cast<const uint4*>(stage_y + mm * kBM + n8);
+        }
+      } else {
+        const int n = n0 + r;
+        if (n < N)
+          for (int mm = 0; mm < slice; ++mm)
+            if (m0 + mm < M) y[int64_t(m0 + mm) * N + n] = stage_y[mm * kBM + r];
+      }
+    }
+    // no CTA leaves while another may still be writing into it
+    cluster_sync();
+    ptx::tc_fence_before();
+    __syncthreads();
+  }
+
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
@@ -543,16 +705,22 @@ qlin_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, 
 
 template <int BITS, typename AT, int BN>
 qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, const void* biases,
-                      void* y, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+                      void* y, int64_t M, int64_t N, int64_t K, int split, cudaStream_t st) {
   using L = Layout<BITS, BN>;
   constexpr int kMaxSmem = 227 * 1024;
   constexpr int kBarBytes = 512;
   // (kDequantGroups + 2) barriers per stage (at most 8), two pairs of
   // accumulator barriers, the teardown barrier and the TMEM address slot
-  static_assert((kDequantGroups + 2) * 8 * 8 + 4 * 8 + 8 + 4 <= kBarBytes, "barrier block");
+  static_assert((kDequantGroups + 2) * 8 * 8 + 4 * 8 + 8 + 8 + 4 <= kBarBytes, "barrier block");
   const int stages =
       std::min(std::min(8, L::kMaxStages), (kMaxSmem - 1024 - kBarBytes) / L::kStageBytes);
   if (stages < 2) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: tile does not fit");
+  // split-K: slices of at least 16 columns, and the receive buffer of the
+  // reduction fits in the ring
+  if (split > 1 && (BN / split < 16 || BN % split != 0 ||
+                    (split - 1) * kBM * (BN / split) * 4 + (BN / split) * kBM * 2 >
+                        stages * L::kStageBytes))
+    split = 1;
   const size_t smem = size_t(stages) * L::kStageBytes + 1024 + kBarBytes;
   // TMEM columns: the accumulators and one A slot per stage, rounded up to a
   // power of two (tcgen05.alloc); at most 512
@@ -600,49 +768,82 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
   }
   const int64_t tiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
   if (tiles > (int64_t(1) << 30)) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: too many tiles");
-  const int grid = int(std::min<int64_t>(tiles, sm_count()));  // persistent: one CTA per SM
-  kern<<<grid, kThreads, smem, st>>>(tm_x, tm_w, tm_s, tm_b, static_cast<const AT*>(scales),
-                                     static_cast<const AT*>(biases), static_cast<AT*>(y), int(M),
-                                     int(N), int(K), stages, tmem_cols);
+  // persistent (one CTA per SM) or, split-K, one cluster of `split` CTAs per tile
+  const int64_t grid = split > 1 ? tiles * split : std::min<int64_t>(tiles, sm_count());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid), 1u, 1u);
+  cfg.blockDim = dim3(unsigned(kThreads), 1u, 1u);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = split > 1 ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, kern, tm_x, tm_w, tm_s, tm_b, static_cast<const AT*>(scales),
+      static_cast<const AT*>(biases), static_cast<AT*>(y), int(M), int(N), int(K), stages,
+      tmem_cols, split);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(QLIN_ERR_CUDA, "qmm_kernel launch: %s", cudaGetErrorString(e));
+  }
   return check_launch("qmm_kernel");
 }
 
 template <int BITS, typename AT>
 qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
-  // Token tile: pick the BN with the smallest estimated time, waves of
-  // persistent tiles x stages per tile x time per stage.  A stage's time is
-  // set by the 128 x BN x 64 MMA for large BN and by a fixed floor (the TMA
-  // requests and the dequantisation of the 128 x 64 weight tile, the same for
-  // every BN) for small BN; measured on GB300 as about 0.40 us at BN = 256
-  // and 0.27-0.30 us at BN <= 128.  Ties go to the larger tile.
+  // Token tile and split-K factor: the pair with the smallest estimated time,
+  // waves of tiles x stages per CTA x time per stage, + the reduction when K
+  // is split.  Measured on GB300, a stage takes about 0.43 us whatever BN:
+  // a 128 x N x 16 MMA takes about the same time for every N up to 256, and
+  // the stage's tcgen05.commit adds a fixed cost.  So wider tiles are free and
+  // narrower ones only pay when they remove a wave.  K is split over a
+  // cluster of 2 or 4 CTAs only when the split tiles fit on the SMs at once
+  // and leave each CTA at least 4 stages; the reduction costs about 2.5 us +
+  // 0.045 us per accumulator column a CTA sends.  Ties go to the larger tile.
   int max_bn = 16;
   while (max_bn < 256 && max_bn < M) max_bn <<= 1;
   const int64_t sms = sm_count();
   const int64_t n_tiles = (N + kBM - 1) / kBM;
-  int bn = max_bn;
+  const int64_t kb_count = K / kBK;
+  int bn = max_bn, split = 1;
   double best = -1.0;
   for (int cand = max_bn; cand >= 16; cand >>= 1) {
     const int64_t tiles = n_tiles * ((M + cand - 1) / cand);
-    const int64_t waves = (tiles + sms - 1) / sms;
-    const double t_stage = std::max(0.27, 0.40 * cand / 256.0);
-    const double cost = double(waves) * t_stage;
-    if (best < 0.0 || cost < best * 0.97) {
-      best = cost;
-      bn = cand;
+    const double t_stage = 0.43;
+    for (int sp = 1; sp <= 4; sp *= 2) {
+      if (sp > 1 && (tiles * sp > sms || kb_count < 4 * sp || cand / sp < 16)) continue;
+      const int64_t waves = (tiles * sp + sms - 1) / sms;
+      // the reduction: about 2.5 us + 0.045 us per column each CTA sends
+      const double cost = double(waves) * double((kb_count + sp - 1) / sp) * t_stage +
+                          (sp > 1 ? 2.5 + 0.045 * cand * (sp - 1) / sp : 0.0);
+      if (best < 0.0 || cost < best * 0.97) {
+        best = cost;
+        bn = cand;
+        split = sp;
+      }
     }
   }
-  // QLIN_QMM_BN (16, 32, 64, 128 or 256) overrides the choice, for tuning
+  // QLIN_QMM_BN (16, 32, 64, 128 or 256) and QLIN_QMM_SPLIT (1, 2 or 4)
+  // override the choice, for tuning
   if (const char* env = std::getenv("QLIN_QMM_BN")) {
     const int v = std::atoi(env);
     if (v == 16 || v == 32 || v == 64 || v == 128 || v == 256) bn = v;
   }
+  if (const char* env = std::getenv("QLIN_QMM_SPLIT")) {
+    const int v = std::atoi(env);
+    if (v == 1 || v == 2 || v == 4) split = v;
+  }
   switch (bn) {
-    case 16: return launch_bn<BITS, AT, 16>(x, wq, scales, biases, y, M, N, K, st);
-    case 32: return launch_bn<BITS, AT, 32>(x, wq, scales, biases, y, M, N, K, st);
-    case 64: return launch_bn<BITS, AT, 64>(x, wq, scales, biases, y, M, N, K, st);
-    case 128: return launch_bn<BITS, AT, 128>(x, wq, scales, biases, y, M, N, K, st);
-    default: return launch_bn<BITS, AT, 256>(x, wq, scales, biases, y, M, N, K, st);
+    case 16: return launch_bn<BITS, AT, 16>(x, wq, scales, biases, y, M, N, K, split, st);
+    case 32: return launch_bn<BITS, AT, 32>(x, wq, scales, biases, y, M, N, K, split, st);
+    case 64: return launch_bn<BITS, AT, 64>(x, wq, scales, biases, y, M, N, K, split, st);
+    case 128: return launch_bn<BITS, AT, 128>(x, wq, scales, biases, y, M, N, K, split, st);
+    default: return launch_bn<BITS, AT, 256>(x, wq, scales, biases, y, M, N, K, split, st);
   }
 }
 

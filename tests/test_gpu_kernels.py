@@ -113,6 +113,9 @@ QMM_CASES = [
     # random-sign data guarantees at K of a few hundred or more, not at K ~ 100
     (768, 8192, 128, 8, "f16"), (768, 8192, 512, 4, "bf16"), (640, 4096, 256, 4, "f16"),
     (1100, 8200, 512, 8, "bf16"),
+    # few tiles: K split over a cluster of 4 (f16, bf16, ragged M and N) or 2
+    (512, 2048, 8192, 4, "f16"), (100, 384, 4096, 8, "bf16"), (300, 1000, 2048, 4, "f16"),
+    (32, 8192, 2048, 4, "f16"),
 ]
 
 
@@ -125,6 +128,48 @@ def test_qmm_parity(dev, m, n, k, bits, dt):
     torch.cuda.synchronize()
     assert canaries_intact(buf)
     assert_within_tolerance(y, ref, f"qmm m={m} n={n} k={k} b={bits} {dt}")
+
+
+@pytest.fixture
+def qmm_tile(monkeypatch):
+    """Force qmm's token tile and split-K factor (QLIN_QMM_BN / _SPLIT)."""
+    def force(bn, split):
+        monkeypatch.setenv("QLIN_QMM_BN", str(bn))
+        monkeypatch.setenv("QLIN_QMM_SPLIT", str(split))
+    return force
+
+
+@pytest.mark.parametrize("bn,split", [(128, 1), (128, 2), (128, 4), (256, 4), (64, 2)])
+def test_qmm_split_k_factors(dev, qmm_tile, bn, split):
+    """Each split of K over a cluster, summed through distributed shared
+    memory, stays within the tolerance of the oracle."""
+    m, n, k, bits, dt = 200, 640, 2048, 8, "f16"
+    w, x, ref = case(4100 + bn + split, m, n, k, bits, dt)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    qmm_tile(bn, split)
+    buf, y = guarded((m, n), TORCH_DT[dt], dev)
+    q.qmm(x.to(dev), wq, sc, bi, bits, out=y)
+    torch.cuda.synchronize()
+    assert canaries_intact(buf)
+    assert_within_tolerance(y, ref, f"qmm split bn={bn} split={split}")
+    assert q.device_status() == 0
+
+
+@pytest.mark.parametrize("bits,dt", [(4, "f16"), (8, "bf16")])
+def test_one_hot_rows_exact_under_split_k(dev, qmm_tile, bits, dt):
+    """With x = e_k only one CTA of a split cluster holds the nonzero term;
+    the others contribute exact zeros, so the sum is still bit-identical to
+    the materialised reconstruction."""
+    n, k = 260, 512
+    w = S.weights_f32(78, n, k)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    cols = np.array([0, 1, 7, 63, 64, 200, 255, 256, 511])
+    x = torch.zeros((cols.size, k), dtype=TORCH_DT[dt])
+    x[np.arange(cols.size), cols] = 1
+    qmm_tile(64, 4)
+    y = q.qmm(x.to(dev), wq, sc, bi, bits)
+    w_hat = q.dequant(wq, sc, bi, bits)
+    assert torch.equal(y.cpu(), w_hat[:, cols].t().contiguous().cpu())
 
 
 @pytest.mark.parametrize("fn", ["qmv", "qmm"])
