@@ -235,9 +235,10 @@ int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
     if (v >= 1) return v;
   }
   // Measured on GB300 (batched-decode sweep, 4-bit, bf16, L2 flushed): the
-  // tensor-core kernel overtakes the CUDA-core one at M = 8 when N >= K
-  // (8192 x 2048) and at M = 16 when K > N (2048 x 8192).
-  return K > N ? 16 : 8;
+  // tensor-core kernel (wide token tiles, K split over a cluster) overtakes
+  // the CUDA-core one at M = 8 when N >= K (8192 x 2048: 16.4 vs 20.5 us) and
+  // at M = 4 when K > N (2048 x 8192: 22.5 vs 24.6 us).
+  return K > N ? 4 : 8;
 }
 
 qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,

@@ -805,8 +805,10 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
   // cluster of 2 or 4 CTAs only when the split tiles fit on the SMs at once
   // and leave each CTA at least 4 stages; the reduction costs about 2.5 us +
   // 0.045 us per accumulator column a CTA sends.  Ties go to the larger tile.
-  int max_bn = 16;
-  while (max_bn < 256 && max_bn < M) max_bn <<= 1;
+  // Tiles wider than the batch are candidates too: the rows past M are
+  // zero-filled by the TMA without memory traffic, cost the MMA nothing, and
+  // a wider tile can be split over more CTAs.
+  const int max_bn = 256;
   const int64_t sms = sm_count();
   const int64_t n_tiles = (N + kBM - 1) / kBM;
   const int64_t kb_count = K / kBK;
