@@ -593,7 +593,8 @@ def profile_case(which: str, launches: int = 3):
     kernel on one workload shape (no timing, no oracle).
       qmv: the lm_head of the decode step (M=1, 128256x2048, 8-bit, f16),
            279 MB of packed weights (above the L2 size);
-      qmm: M=2048, N=8192, K=2048, 4-bit, f16 (the largest prefill case)."""
+      qmm: M=2048, N=8192, K=2048, 4-bit, f16 (the largest prefill case);
+      qmm_split: M=512, N=2048, K=8192, 4-bit (K split over 4-CTA clusters)."""
     import torch
 
     import int8_qmv_qmm_gb300 as q
@@ -604,7 +605,8 @@ def profile_case(which: str, launches: int = 3):
     cases = {"qmv": (1, 128256, 2048, 8, q.qmv), "qmv_o": (1, 2048, 2048, 8, q.qmv),
              "qmv_gate_up": (1, 16384, 2048, 8, q.qmv), "qmv_down": (1, 2048, 8192, 8, q.qmv),
              "qmm": (2048, 8192, 2048, 4, q.qmm), "qmm8": (2048, 8192, 2048, 8, q.qmm),
-             "qmm_sq": (2048, 2048, 2048, 8, q.qmm)}
+             "qmm_sq": (2048, 2048, 2048, 8, q.qmm),
+             "qmm_split": (512, 2048, 8192, 4, q.qmm)}
     m, n, k, bits, fn = cases[which]
     w = torch.from_numpy(S.weights_f32(7, n, k)).to(dev)
     wq, sc, bi = q.quantize_affine(w, bits, sdtype=torch.float16)
@@ -630,7 +632,7 @@ def main():
     ap.add_argument("--no-qmm", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["qmv", "qmv_o", "qmv_gate_up", "qmv_down", "qmm",
-                                          "qmm8", "qmm_sq"],
+                                          "qmm8", "qmm_sq", "qmm_split"],
                     help="run a small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
     if args.profile:
