@@ -204,11 +204,13 @@ qlin_status qlin_qmv_chain_static(const void* x0, const qlin_link* links, int n_
 
 /*
  * The same product on the tensor cores (batched decode and prefill): packed
- * tiles are staged into shared memory by TMA, dequantised there to dtype
- * (bit-identical to qlin_dequant's dtype output) and fed to tcgen05 MMA with
- * f32 accumulators in tensor memory.  Same arguments and result contract as
- * qlin_qmv.  Extra requirement: K % 64 == 0 (always true for group 64) and
- * x, wq 16-byte aligned.
+ * tiles are staged into shared memory by TMA, dequantised to dtype
+ * (bit-identical to qlin_dequant's dtype output) into tensor memory as the
+ * A operand of tcgen05 MMAs with f32 accumulators in tensor memory; when the
+ * output has few tiles, K is split over a thread-block cluster and the
+ * partial sums are added through distributed shared memory (no workspace).
+ * Same arguments and result contract as qlin_qmv.  Extra requirement:
+ * K % 64 == 0 (always true for group 64) and x, wq 16-byte aligned.
  */
 qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
@@ -223,6 +225,29 @@ qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
 
 /* Smallest M for which qlin_linear picks the tensor-core path (measured). */
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits);
+
+/*
+ * qlin_linear with a linear layer's epilogue:
+ *
+ *   y[m][n] = RNE_ydtype( sum_k x[m][k] * w_hat[n][k]  +  layer_bias[n] )
+ *
+ * layer_bias: dtype [N] (the activation dtype), added to the f32 accumulator
+ *   before the single final rounding; NULL for no bias.  (This is the layer's
+ *   own bias vector, not the quantisation biases of the packed format.)
+ * y_dtype: QLIN_F32 (y is float [M][N], 4-byte aligned, no rounding) or the
+ *   activation dtype (y as in qlin_linear).
+ * The pages' ExecuTorch stack ships a 4-bit linear with bias ("feat: extend
+ * the fused low-precision path to the Metal target", results table); the
+ * f32 output serves callers that keep the residual stream in f32.
+ *
+ * Errors: as qlin_linear; y_dtype other than QLIN_F32 or dtype is
+ * QLIN_ERR_UNSUPPORTED; layer_bias not 2-byte or an f32 y not 4-byte aligned
+ * is QLIN_ERR_MISALIGNED.
+ */
+qlin_status qlin_linear_ex(const void* x, const uint32_t* wq, const void* scales,
+                           const void* biases, const void* layer_bias, void* y, int64_t M,
+                           int64_t N, int64_t K, int bits, int group_size, qlin_dtype dtype,
+                           qlin_dtype y_dtype, void* stream);
 
 /*
  * Read and clear the device status words of the current device (synchronises

@@ -48,6 +48,7 @@ _SIGNATURES = {
     "qlin_qmv_ex": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [ctypes.c_uint, _c_vp]),
     "qlin_qmm": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_linear": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
+    "qlin_linear_ex": (_c_int, [_c_vp] * 6 + [_c_i64] * 3 + [_c_int] * 4 + [_c_vp]),
     "qlin_crossover_m": (_c_i64, [_c_i64, _c_i64, _c_int]),
     "qlin_qmv_chain_workspace_size": (ctypes.c_size_t, [_c_int]),
     "qlin_qmv_chain": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int, _c_vp,
@@ -176,9 +177,34 @@ def qmm(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
     return _matmul("qlin_qmm", x, wq, scales, biases, bits, group_size, out)
 
 
-def linear(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
-    """qmv below the measured crossover M, qmm above it."""
-    return _matmul("qlin_linear", x, wq, scales, biases, bits, group_size, out)
+def linear(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None, bias=None,
+           out_dtype=None):
+    """qmv below the measured crossover M, qmm above it.
+
+    bias: optional [N] tensor in the activation dtype (a linear layer's own
+    bias, added before the final rounding); out_dtype: torch.float32 for a
+    float32 result, else the activation dtype (qlin_linear_ex)."""
+    if bias is None and (out_dtype is None or out_dtype == x.dtype):
+        return _matmul("qlin_linear", x, wq, scales, biases, bits, group_size, out)
+    _need_cuda(x, wq, scales, biases)
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D [M, K]")
+    m, k = x.shape
+    n = wq.shape[0]
+    if wq.shape[1] * 32 // bits != k:
+        raise ValueError("wq does not match K")
+    if bias is not None:
+        _need_cuda(bias)
+        if bias.shape != (n,) or bias.dtype != x.dtype:
+            raise ValueError("bias must be [N] in the activation dtype")
+    out_dtype = out_dtype or x.dtype
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=x.device)
+    _need_cuda(out)
+    _check(lib().qlin_linear_ex(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(bias),
+                                _ptr(out), m, n, k, bits, group_size, _DTYPE_CODE[x.dtype],
+                                _DTYPE_CODE[out_dtype], _stream(x)))
+    return out
 
 
 def chain_workspace(n_links: int, device) -> torch.Tensor:

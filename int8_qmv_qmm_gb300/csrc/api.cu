@@ -66,12 +66,15 @@ qlin_status check_act_dtype(qlin_dtype d, const char* what) {
 
 using MatmulLauncher = qlin_status (*)(const void*, const uint32_t*, const void*, const void*,
                                        void*, int64_t, int64_t, int64_t, int, qlin_dtype,
-                                       unsigned, cudaStream_t);
+                                       unsigned, const Epilogue&, cudaStream_t);
+
+const Epilogue kPlainEpilogue = {nullptr, 0};
 
 qlin_status matmul_entry(const char* name, MatmulLauncher launch, const void* x,
                          const uint32_t* wq, const void* scales, const void* biases, void* y,
                          int64_t M, int64_t N, int64_t K, int bits, int group_size,
-                         qlin_dtype dtype, unsigned flags, void* stream) {
+                         qlin_dtype dtype, unsigned flags, void* stream,
+                         const Epilogue& ep = kPlainEpilogue) {
   qlin_status s = check_format(N, K, bits, group_size);
   if (s != QLIN_OK) return s;
   if (flags & ~unsigned(QLIN_OVERLAP_PREVIOUS))
@@ -84,9 +87,13 @@ qlin_status matmul_entry(const char* name, MatmulLauncher launch, const void* x,
     return fail(QLIN_ERR_INVALID_ARG, "%s: null pointer argument", name);
   if (!aligned(x, 16) || !aligned(wq, 16))
     return fail(QLIN_ERR_MISALIGNED, "%s: x and wq must be 16-byte aligned", name);
-  if (!aligned(scales, 2) || !aligned(biases, 2) || !aligned(y, 2))
-    return fail(QLIN_ERR_MISALIGNED, "%s: scales, biases and y must be 2-byte aligned", name);
-  return launch(x, wq, scales, biases, y, M, N, K, bits, dtype, flags,
+  if (!aligned(scales, 2) || !aligned(biases, 2) || !aligned(y, ep.y_f32 ? 4 : 2))
+    return fail(QLIN_ERR_MISALIGNED,
+                "%s: scales and biases must be 2-byte aligned, y %d-byte aligned", name,
+                ep.y_f32 ? 4 : 2);
+  if (ep.bias && !aligned(ep.bias, 2))
+    return fail(QLIN_ERR_MISALIGNED, "%s: the layer bias must be 2-byte aligned", name);
+  return launch(x, wq, scales, biases, y, M, N, K, bits, dtype, flags, ep,
                 reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -250,6 +257,23 @@ qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
                         group_size, dtype, 0u, stream);
   return matmul_entry("qlin_linear", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,
                       group_size, dtype, 0u, stream);
+}
+
+qlin_status qlin_linear_ex(const void* x, const uint32_t* wq, const void* scales,
+                           const void* biases, const void* layer_bias, void* y, int64_t M,
+                           int64_t N, int64_t K, int bits, int group_size, qlin_dtype dtype,
+                           qlin_dtype y_dtype, void* stream) {
+  g_last_error[0] = 0;
+  if (y_dtype != QLIN_F32 && y_dtype != dtype)
+    return fail(QLIN_ERR_UNSUPPORTED,
+                "qlin_linear_ex: y dtype %d must be float32 or the activation dtype %d",
+                int(y_dtype), int(dtype));
+  const Epilogue ep = {layer_bias, y_dtype == QLIN_F32 ? 1 : 0};
+  if (M < qlin_crossover_m(N, K, bits))
+    return matmul_entry("qlin_linear_ex", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
+                        group_size, dtype, 0u, stream, ep);
+  return matmul_entry("qlin_linear_ex", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,
+                      group_size, dtype, 0u, stream, ep);
 }
 
 qlin_status qlin_device_status(int* flags) {

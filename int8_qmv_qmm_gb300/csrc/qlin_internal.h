@@ -23,12 +23,20 @@ qlin_status launch_quantize(const float* w, int64_t N, int64_t K, int bits, qlin
 qlin_status launch_dequant(const uint32_t* wq, const void* scales, const void* biases, int64_t N,
                            int64_t K, int bits, qlin_dtype sdtype, qlin_dtype out_dtype,
                            void* w_out, cudaStream_t st);
+// A linear layer's epilogue: the layer bias (activation dtype [N], or null)
+// added before the final rounding, and float32 output instead of the
+// activation dtype.
+struct Epilogue {
+  const void* bias;
+  int y_f32;
+};
+
 qlin_status launch_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, cudaStream_t st);
+                       unsigned flags, const Epilogue& ep, cudaStream_t st);
 qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, cudaStream_t st);
+                       unsigned flags, const Epilogue& ep, cudaStream_t st);
 
 qlin_status launch_qmv_chain(const void* x0, const qlin_link* links, int n_links, int bits,
                              qlin_dtype dtype, void* ws, cudaStream_t st);

@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_b,
                const AT* __restrict__ scales, const AT* __restrict__ biases, AT* __restrict__ y,
-               int M, int N, int K, int stages, int tmem_cols, int split) {
+               int M, int N, int K, int stages, int tmem_cols, int split,
+               const AT* __restrict__ layer_bias, int y_f32) {
   using L = Layout<BITS, BN>;
   using G = Geo<BITS>;
   extern __shared__ uint8_t smem_raw[];
@@ -510,6 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       if (split > 1) break;  // partial accumulator: reduced across the cluster below
       const int n = (t % n_tiles) * kBM + r, m0 = (t / n_tiles) * BN;
+      // a linear layer's bias (qlin_linear_ex) joins the f32 sum before the rounding
+      const float lb = layer_bias && n < N ? Act<AT>::to_f32(layer_bias[n]) : 0.0f;
       const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(buf * BN);
       // batches of up to 64 columns: four loads, one wait (a TMEM load's
       // latency per batch, not per 16 columns); the accumulator is handed
@@ -532,7 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < kBatch; ++j) {
             const int m = m0 + c0 + j;
-            if (m < M) y[int64_t(m) * N + n] = Act<AT>::from_f32_rn(__uint_as_float(v[j]));
+            const float o = __uint_as_float(v[j]) + lb;
+            if (m < M) {
+              if (y_f32)
+                reinterpret_cast<float*>(y)[int64_t(m) * N + n] = o;
+              else
+                y[int64_t(m) * N + n] = Act<AT>::from_f32_rn(o);
+            }
           }
         }
       }
@@ -602,6 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = t_first;
       const int n0 = (t % n_tiles) * kBM, m0 = (t / n_tiles) * BN + rank * slice;
       AT* stage_y = reinterpret_cast<AT*>(gbase + (split - 1) * slice * kBM * 4);
+      const float lb = layer_bias && n0 + r < N ? Act<AT>::to_f32(layer_bias[n0 + r]) : 0.0f;
 #pragma unroll 1
       for (int c0 = 0; c0 < slice; c0 += batch) {
         uint32_t v[kRBatch];
@@ -625,6 +635,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               a3 += p.w;
             }
             const int mm = c0 + 4 * q;
+            a0 += lb;
+            a1 += lb;
+            a2 += lb;
+            a3 += lb;
+            if (y_f32) {
+              // float32 output: stored directly, rows along n
+              float* yf = reinterpret_cast<float*>(y);
+              const int n = n0 + r;
+              if (n < N) {
+                if (m0 + mm < M) yf[int64_t(m0 + mm) * N + n] = a0;
+                if (m0 + mm + 1 < M) yf[int64_t(m0 + mm + 1) * N + n] = a1;
+                if (m0 + mm + 2 < M) yf[int64_t(m0 + mm + 2) * N + n] = a2;
+                if (m0 + mm + 3 < M) yf[int64_t(m0 + mm + 3) * N + n] = a3;
+              }
+              continue;
+            }
             stage_y[(mm + 0) * kBM + r] = Act<AT>::from_f32_rn(a0);
             stage_y[(mm + 1) * kBM + r] = Act<AT>::from_f32_rn(a1);
             stage_y[(mm + 2) * kBM + r] = Act<AT>::from_f32_rn(a2);
@@ -632,7 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // the four epilogue warps' rows are all staged
+      // the four epilogue warps' rows are all staged (the same branch for
+      // all four: y_f32 is a kernel argument)
+      if (!y_f32) {
       asm volatile("bar.sync 2, 128;" ::: "memory");
       const int et = threadIdx.x - (2 + kDequantWarps) * 32;  // 0..127
       const bool vec = N % 8 == 0 && n0 + kBM <= N &&
@@ -651,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n < N)
           for (int mm = 0; mm < slice; ++mm)
             if (m0 + mm < M) y[int64_t(m0 + mm) * N + n] = stage_y[mm * kBM + r];
+      }
       }
     }
     // no CTA leaves while another may still be writing into it
@@ -705,7 +734,8 @@ qlin_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, 
 
 template <int BITS, typename AT, int BN>
 qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, const void* biases,
-                      void* y, int64_t M, int64_t N, int64_t K, int split, cudaStream_t st) {
+                      void* y, int64_t M, int64_t N, int64_t K, int split, const Epilogue& ep,
+                      cudaStream_t st) {
   using L = Layout<BITS, BN>;
   constexpr int kMaxSmem = 227 * 1024;
   constexpr int kBarBytes = 512;
@@ -785,7 +815,7 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
   const cudaError_t e = cudaLaunchKernelEx(
       &cfg, kern, tm_x, tm_w, tm_s, tm_b, static_cast<const AT*>(scales),
       static_cast<const AT*>(biases), static_cast<AT*>(y), int(M), int(N), int(K), stages,
-      tmem_cols, split);
+      tmem_cols, split, static_cast<const AT*>(ep.bias), ep.y_f32);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(QLIN_ERR_CUDA, "qmm_kernel launch: %s", cudaGetErrorString(e));
@@ -795,7 +825,8 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
 
 template <int BITS, typename AT>
 qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, const void* biases,
-                     void* y, int64_t M, int64_t N, int64_t K, cudaStream_t st) {
+                     void* y, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
+                     cudaStream_t st) {
   // Token tile and split-K factor: the pair with the smallest estimated time,
   // waves of tiles x stages per CTA x time per stage, + the reduction when K
   // is split.  Measured on GB300, a stage takes about 0.43 us whatever BN:
@@ -841,11 +872,11 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
     if (v == 1 || v == 2 || v == 4) split = v;
   }
   switch (bn) {
-    case 16: return launch_bn<BITS, AT, 16>(x, wq, scales, biases, y, M, N, K, split, st);
-    case 32: return launch_bn<BITS, AT, 32>(x, wq, scales, biases, y, M, N, K, split, st);
-    case 64: return launch_bn<BITS, AT, 64>(x, wq, scales, biases, y, M, N, K, split, st);
-    case 128: return launch_bn<BITS, AT, 128>(x, wq, scales, biases, y, M, N, K, split, st);
-    default: return launch_bn<BITS, AT, 256>(x, wq, scales, biases, y, M, N, K, split, st);
+    case 16: return launch_bn<BITS, AT, 16>(x, wq, scales, biases, y, M, N, K, split, ep, st);
+    case 32: return launch_bn<BITS, AT, 32>(x, wq, scales, biases, y, M, N, K, split, ep, st);
+    case 64: return launch_bn<BITS, AT, 64>(x, wq, scales, biases, y, M, N, K, split, ep, st);
+    case 128: return launch_bn<BITS, AT, 128>(x, wq, scales, biases, y, M, N, K, split, ep, st);
+    default: return launch_bn<BITS, AT, 256>(x, wq, scales, biases, y, M, N, K, split, ep, st);
   }
 }
 
@@ -853,13 +884,13 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
 
 qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, cudaStream_t st) {
+                       unsigned flags, const Epilogue& ep, cudaStream_t st) {
   (void)flags;
   if (dtype == QLIN_F16)
-    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, st)
-                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, st);
-  return bits == 4 ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, st)
-                   : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, st);
+    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, ep, st)
+                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, ep, st);
+  return bits == 4 ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, ep, st)
+                   : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, ep, st);
 }
 
 cudaError_t qmm_take_device_status(unsigned* flags) {

@@ -55,6 +55,7 @@ struct Shape {
   int stages;       // ring depth
   int stage_bytes;  // bytes of one stage (weights, then scales and biases)
   unsigned flags;
+  Epilogue ep;      // layer bias and f32 output (qlin_linear_ex)
 };
 
 // MODE 0: generic k-tiles, scales read from global memory; 1: generic k-tiles,
@@ -201,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
         ++round;
       }
     }
-    store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, y, N);
+    store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, static_cast<void*>(y), N,
+                          static_cast<const AT*>(sh.ep.bias), sh.ep.y_f32 != 0);
   }
 }
 
@@ -330,9 +332,11 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
 
 template <int BITS, typename AT>
 qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, const void* biases,
-                     void* y, int64_t M, int64_t N, int64_t K, unsigned flags, cudaStream_t st) {
+                     void* y, int64_t M, int64_t N, int64_t K, unsigned flags,
+                     const Epilogue& ep, cudaStream_t st) {
   Shape sh{};
   sh.flags = flags;
+  sh.ep = ep;
   sh.M = int(M);
   sh.N = int(N);
   sh.K = int(K);
@@ -350,12 +354,13 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
 
 qlin_status launch_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, cudaStream_t st) {
+                       unsigned flags, const Epilogue& ep, cudaStream_t st) {
   if (dtype == QLIN_F16)
-    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, flags, st)
-                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, flags, st);
-  return bits == 4 ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, st)
-                   : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, st);
+    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, flags, ep, st)
+                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, flags, ep, st);
+  return bits == 4 ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, ep, st)
+                   : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, ep,
+                                                st);
 }
 
 cudaError_t qmv_take_device_status(unsigned* flags) {

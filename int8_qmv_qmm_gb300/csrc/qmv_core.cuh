@@ -354,22 +354,35 @@ __device__ __forceinline__ void accumulate_fixed(const uint8_t* stage, int w0, i
 // leading dimension ldy).  Returns true on the lanes that stored a value.
 template <int MT, int R, typename AT>
 __device__ __forceinline__ bool store_rows(float2 (&acc)[R][MT], int lane, int row0, int m0,
-                                           int N, int M, AT* __restrict__ y, int64_t ldy) {
+                                           int N, int M, void* __restrict__ y, int64_t ldy,
+                                           const AT* __restrict__ layer_bias, bool y_f32) {
   constexpr int kV = R * MT;
   float v[kV];
 #pragma unroll
   for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int mm = 0; mm < MT; ++mm) v[r * MT + mm] = acc[r][mm].x + acc[r][mm].y;
-  const float total = butterfly_sum<kV>(v, lane);
+  float total = butterfly_sum<kV>(v, lane);
   constexpr int kLanesPerValue = 32 / kV;
   const int vi = lane / kLanesPerValue;
   const int row = row0 + vi / MT, m = m0 + vi % MT;
   if ((lane % kLanesPerValue) == 0 && row < N && m < M) {
-    y[int64_t(m) * ldy + row] = Act<AT>::from_f32_rn(total);
+    // a linear layer's bias joins the f32 sum before the one rounding
+    if (layer_bias) total += Act<AT>::to_f32(layer_bias[row]);
+    if (y_f32)
+      static_cast<float*>(y)[int64_t(m) * ldy + row] = total;
+    else
+      static_cast<AT*>(y)[int64_t(m) * ldy + row] = Act<AT>::from_f32_rn(total);
     return true;
   }
   return false;
+}
+
+template <int MT, int R, typename AT>
+__device__ __forceinline__ bool store_rows(float2 (&acc)[R][MT], int lane, int row0, int m0,
+                                           int N, int M, AT* __restrict__ y, int64_t ldy) {
+  return store_rows<MT, R, AT>(acc, lane, row0, m0, N, M, static_cast<void*>(y), ldy,
+                               static_cast<const AT*>(nullptr), false);
 }
 
 }  // namespace qmvcore

@@ -245,6 +245,20 @@ def matmul_ref(x, w_hat):
     return x64 @ w64.T, np.abs(x64) @ np.abs(w64).T
 
 
+def matmul_bias_ref(x, w_hat, layer_bias):
+    """A linear layer: y_ref = x . w_hat^T + layer_bias in float64, and the
+    tolerance base A = |x| . |w_hat|^T + |layer_bias| (the bias is one more
+    term of each output's sum).
+
+    layer_bias[N] is a linear layer's own bias vector (the ExecuTorch stack's
+    "4-bit linear with bias": "feat: extend the fused low-precision path to
+    the Metal target", results table), not the quantisation biases.
+    """
+    y_ref, a_ref = matmul_ref(x, w_hat)
+    b64 = np.asarray(layer_bias, dtype=np.float64)
+    return y_ref + b64[None, :], a_ref + np.abs(b64)[None, :]
+
+
 TOL_REL = 2e-3
 TOL_ABS = 1e-5
 

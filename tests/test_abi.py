@@ -100,6 +100,27 @@ def test_quantize_and_dequant_validation(L):
                           vp(FAKE), None) == INVALID
 
 
+def test_linear_ex_validation(L):
+    vp = ctypes.c_void_p
+
+    def call(y_dt=q.QLIN_F32, lb=FAKE, y=FAKE, dt=q.QLIN_F16, M=1):
+        return L.qlin_linear_ex(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(lb), vp(y), M, 300,
+                                512, 4, 64, dt, y_dt, None)
+
+    # the output is float32 or the activation dtype
+    assert call(y_dt=q.QLIN_BF16) == UNSUPPORTED
+    assert call(y_dt=q.QLIN_F16, dt=q.QLIN_BF16) == UNSUPPORTED
+    # a float32 y needs 4-byte alignment, the layer bias 2-byte alignment
+    assert call(y=FAKE + 2) == MISALIGNED
+    assert call(lb=FAKE + 1) == MISALIGNED
+    assert call(M=600, lb=FAKE + 1) == MISALIGNED
+    # the format checks still come first
+    assert L.qlin_linear_ex(vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE), vp(0), vp(FAKE), 1, 300, 512,
+                            3, 64, q.QLIN_F16, q.QLIN_F32, None) == UNSUPPORTED
+    # empty product: nothing launched
+    assert call(M=0) == OK
+
+
 def test_device_status_rejects_null(L):
     assert L.qlin_device_status(None) == INVALID
 

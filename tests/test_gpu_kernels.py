@@ -199,6 +199,42 @@ def test_linear_dispatches_both_paths(dev):
         assert_within_tolerance(y, ref, f"linear m={m}")
 
 
+@pytest.mark.parametrize("m,n,k,bits,dt", [
+    (1, 300, 512, 4, "f16"), (3, 1029, 2048, 8, "bf16"),        # qmv
+    (40, 301, 512, 4, "f16"), (600, 384, 512, 8, "bf16"),        # qmm
+    (512, 2048, 8192, 4, "f16"), (32, 8192, 2048, 4, "bf16"),    # qmm, K split over a cluster
+])
+@pytest.mark.parametrize("with_bias,f32_out", [(True, False), (True, True), (False, True)])
+def test_linear_bias_and_f32_output(dev, m, n, k, bits, dt, with_bias, f32_out):
+    """qlin_linear_ex: a linear layer's bias added before the one rounding, and
+    a float32 result, through whichever kernel the crossover picks."""
+    w, x, ref = case(6100 + m + n, m, n, k, bits, dt)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    rng = np.random.default_rng(6200 + m)
+    b = torch.from_numpy(rng.standard_normal(n).astype(np.float32) * 0.5).to(TORCH_DT[dt])
+    b64 = b.double().numpy() if with_bias else np.zeros(n)
+    y_ref, a_ref = O.matmul_bias_ref(x.double().numpy(), ref["w_hat"], b64)
+    y = q.linear(x.to(dev), wq, sc, bi, bits, bias=b.to(dev) if with_bias else None,
+                 out_dtype=torch.float32 if f32_out else None)
+    torch.cuda.synchronize()
+    assert y.dtype == (torch.float32 if f32_out else TORCH_DT[dt])
+    assert_within_tolerance(y, {"y_ref": y_ref, "a_ref": a_ref},
+                            f"linear_ex m={m} n={n} bias={with_bias} f32={f32_out}")
+    assert q.device_status() == 0
+
+
+def test_linear_f32_output_is_the_unrounded_sum(dev):
+    """The float32 output is the accumulator itself: rounding it to the
+    activation dtype gives the plain call's output bit for bit."""
+    m, n, k, bits, dt = 600, 384, 512, 4, "f16"
+    w, x, _ = case(6300, m, n, k, bits, dt)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    xd = x.to(dev)
+    y16 = q.linear(xd, wq, sc, bi, bits)
+    y32 = q.linear(xd, wq, sc, bi, bits, out_dtype=torch.float32)
+    assert torch.equal(y32.to(torch.float16), y16)
+
+
 def test_empty_batch_is_a_no_op(dev):
     wq = torch.zeros((8, 64), dtype=torch.int32, device=dev)
     sc = torch.zeros((8, 8), dtype=torch.float16, device=dev)

@@ -299,6 +299,49 @@ def test_zero_scale_groups_give_bias_times_group_sum():
     assert np.allclose(r["y_ref"], expect, rtol=0, atol=1e-12)
 
 
+def _bias_bruteforce_errors(fn):
+    """Every output of fn(x, w, b) against a correctly rounded math.fsum of its
+    terms x_k w_nk plus b_n; M != N so a bias added along the wrong axis fails."""
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((3, 40))
+    w = rng.standard_normal((5, 40))
+    b = rng.standard_normal(5) * 4
+    y, a = fn(x, w, b)
+    bad = []
+    for m in range(3):
+        for n in range(5):
+            exact = math.fsum([float(x[m, k] * w[n, k]) for k in range(40)] + [float(b[n])])
+            mag = math.fsum([abs(float(x[m, k] * w[n, k])) for k in range(40)] + [abs(float(b[n]))])
+            if abs(y[m, n] - exact) > 1e-13 * mag or abs(a[m, n] - mag) > 1e-13 * mag:
+                bad.append((m, n))
+    return bad
+
+
+def test_linear_bias_matches_correctly_rounded_sums():
+    assert _bias_bruteforce_errors(O.matmul_bias_ref) == []
+
+
+def test_linear_bias_alone_when_x_is_zero():
+    w = S.weights_f32(12, 6, 128).astype(np.float64)
+    b = np.array([0.5, -0.25, 3.0, 0.0, -7.5, 1e-3])
+    y, a = O.matmul_bias_ref(np.zeros((2, 128)), w, b)
+    assert np.array_equal(y, np.tile(b, (2, 1)))
+    assert np.array_equal(a, np.tile(np.abs(b), (2, 1)))
+
+
+@pytest.mark.parametrize("mutant", ["no_bias", "minus_bias", "bias_on_m"])
+def test_linear_bias_mutations_fail_a_pin(mutant):
+    def fn(x, w, b):
+        y, a = O.matmul_ref(x, w)
+        if mutant == "no_bias":
+            return y, a + np.abs(b)
+        if mutant == "minus_bias":
+            return y - b, a + np.abs(b)
+        # the bias indexed by the token instead of the output row
+        return y + np.resize(b, y.shape[0])[:, None], a + np.abs(b)
+    assert _bias_bruteforce_errors(fn) != []
+
+
 def test_within_tolerance_formula():
     y_ref = np.array([1.0, 1.0, 0.0])
     a = np.array([10.0, 10.0, 0.0])
