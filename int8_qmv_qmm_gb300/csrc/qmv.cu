@@ -60,8 +60,9 @@ struct Shape {
 
 // MODE 0: generic k-tiles, scales read from global memory; 1: generic k-tiles,
 // scales copied into the stage; 2: fixed 2048-code k-tiles with scales copied
-// (the fast path).
-template <int BITS, int MT, int R, typename AT, int MODE>
+// (the fast path).  EPI: a linear layer's epilogue (bias, float32 output) is
+// applied; a separate instance, so the plain path's code is untouched.
+template <int BITS, int MT, int R, typename AT, int MODE, bool EPI>
 __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
     const AT* __restrict__ x, const uint32_t* __restrict__ wq, const AT* __restrict__ scales,
     const AT* __restrict__ biases, AT* __restrict__ y, const Shape sh) {
@@ -202,8 +203,11 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
         ++round;
       }
     }
-    store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, static_cast<void*>(y), N,
-                          static_cast<const AT*>(sh.ep.bias), sh.ep.y_f32 != 0);
+    if constexpr (EPI)
+      store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, static_cast<void*>(y), N,
+                            static_cast<const AT*>(sh.ep.bias), sh.ep.y_f32 != 0);
+    else
+      store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, y, N);
   }
 }
 
@@ -215,10 +219,10 @@ size_t smem_for(const Shape& sh, int MT, int R, int bits) {
          size_t(sh.stages) * 16;
 }
 
-template <int BITS, int MT, int R, typename AT, int MODE>
+template <int BITS, int MT, int R, typename AT, int MODE, bool EPI>
 qlin_status launch_t(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, const Shape& sh, size_t smem, cudaStream_t st) {
-  auto kern = qmv_kernel<BITS, MT, R, AT, MODE>;
+  auto kern = qmv_kernel<BITS, MT, R, AT, MODE, EPI>;
   // per device: attribute set once; occupancy cached per dynamic smem size
   static int attr_dev = -1;
   static size_t occ_smem[8] = {0};
@@ -321,12 +325,17 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
   }
   if (smem > 220 * 1024)
     return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmv: K=%d too large for the staged x", sh.K);
-#define QLIN_QMV_LAUNCH(RR)                                                                  \
-  return mode == 2   ? launch_t<BITS, MT, RR, AT, 2>(x, wq, scales, biases, y, sh, smem, st)  \
-         : mode == 1 ? launch_t<BITS, MT, RR, AT, 1>(x, wq, scales, biases, y, sh, smem, st)  \
-                     : launch_t<BITS, MT, RR, AT, 0>(x, wq, scales, biases, y, sh, smem, st)
-  if (R == 2) QLIN_QMV_LAUNCH(2);
-  QLIN_QMV_LAUNCH(1);
+  const bool epi = sh.ep.bias != nullptr || sh.ep.y_f32;
+#define QLIN_QMV_LAUNCH(RR, E)                                                                  \
+  return mode == 2   ? launch_t<BITS, MT, RR, AT, 2, E>(x, wq, scales, biases, y, sh, smem, st)  \
+         : mode == 1 ? launch_t<BITS, MT, RR, AT, 1, E>(x, wq, scales, biases, y, sh, smem, st)  \
+                     : launch_t<BITS, MT, RR, AT, 0, E>(x, wq, scales, biases, y, sh, smem, st)
+  if (epi) {
+    if (R == 2) QLIN_QMV_LAUNCH(2, true);
+    QLIN_QMV_LAUNCH(1, true);
+  }
+  if (R == 2) QLIN_QMV_LAUNCH(2, false);
+  QLIN_QMV_LAUNCH(1, false);
 #undef QLIN_QMV_LAUNCH
 }
 
