@@ -449,6 +449,57 @@ def time_graph_steps(step, steps, device, dist=None):
     return e0.elapsed_time(e1) * 1e-3
 
 
+def dense_f16_step(q, step, device, steps: int):
+    """The same decode step with every weight resident as dense f16 (built
+    once with qlin_dequant, outside the timed region) and each linear run as
+    torch's F.linear (cuBLAS): the unfused f16 path the packed kernels replace.
+    Same chaining, one CUDA graph, same number of replays."""
+    import torch
+    import torch.nn.functional as F
+
+    ws = [q.dequant(u["wq"], u["scales"], u["biases"], step.bits) for u in step.units]
+    outs = [torch.empty_like(u["out"]) for u in step.units]
+
+    def input_of(i):
+        name = step.units[i]["name"]
+        if i == 0:
+            return step.x0
+        prev = outs[i - 1]
+        if name == "o":
+            return prev[:, :2048]
+        if name == "down":
+            return prev[:, :8192]
+        return prev
+
+    def run():
+        for i in range(len(ws)):
+            torch.matmul(input_of(i), ws[i].t(), out=outs[i])
+
+    run()
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(20_000_000)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(device)
+    t = e0.elapsed_time(e1) * 1e-3 / steps
+    dense_bytes = sum(w.numel() * 2 for w in ws)
+    del ws, outs, g
+    torch.cuda.empty_cache()
+    return {"tokens_per_s": 1.0 / t, "ms_per_step": t * 1e3, "weight_bytes": dense_bytes,
+            "gbs": dense_bytes / t / 1e9, "how": "dense f16 weights, torch F.linear (cuBLAS), "
+            "one CUDA graph of the same 65 chained linears"}
+
+
 def bench_ours(args):
     import torch
 
@@ -505,6 +556,9 @@ def bench_ours(args):
     step.mode = "launches"
     step.capture()
 
+    # ---- the unfused comparator: the same step on dense f16 weights (cuBLAS)
+    dense = dense_f16_step(q, step, device, args.steps)
+
     # ---- end to end through the public API with host buffers
     logits_host = torch.empty((1, step.logits.shape[1]), dtype=torch.float16).pin_memory()
     torch.cuda.synchronize(device)
@@ -554,6 +608,7 @@ def bench_ours(args):
         "chain_mode": {"tokens_per_s": world * args.steps / t_c,
                        "kernel_us": chain_s * 1e6,
                        "kernel_gbs": alg / chain_s / 1e9},
+        "dense_f16_step": dict(dense, packed_speedup=value / world / dense["tokens_per_s"]),
         "qmm": qmm_res,
         "crossover": cross,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,

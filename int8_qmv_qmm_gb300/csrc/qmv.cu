@@ -29,6 +29,7 @@
 // bit and the CTA unwinds after its outstanding copies have landed.
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "device_common.cuh"
 #include "qlin_internal.h"
@@ -287,7 +288,12 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
   // rows per consumer warp: two (x reuse, fewer blocks) when rows are
   // plentiful, one when the launch would otherwise leave SMs idle (four rows
   // per warp needs ~150 registers and halves the resident warps: slower)
-  const int R = sh.N >= 16 * 2 * sms ? 2 : 1;
+  int R = sh.N >= 16 * 2 * sms ? 2 : 1;
+  // QLIN_QMV_R (1 or 2) overrides the rows per warp, for tuning
+  if (const char* env = std::getenv("QLIN_QMV_R")) {
+    const int v = std::atoi(env);
+    if (v == 1 || v == 2) R = v;
+  }
   const int RB = kConsumerWarps * R;
   const bool sb_aligned = (reinterpret_cast<uintptr_t>(scales) % 16) == 0 &&
                           (reinterpret_cast<uintptr_t>(biases) % 16) == 0;
