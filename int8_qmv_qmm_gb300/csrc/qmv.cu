@@ -251,6 +251,12 @@ qlin_status launch_t(const void* x, const uint32_t* wq, const void* scales, cons
     occ_smem[slot] = smem;
     occ_blocks[slot] = b;
   }
+  // QLIN_QMV_CTAS_PER_SM caps the persistent grid below the occupancy limit,
+  // leaving room on each SM for the next launch's CTAs (tuning)
+  if (const char* env = std::getenv("QLIN_QMV_CTAS_PER_SM")) {
+    const int v = std::atoi(env);
+    if (v >= 1 && v < blocks_per_sm) blocks_per_sm = v;
+  }
   const int64_t m_tiles = (sh.M + MT - 1) / MT;
   if (m_tiles > 65535) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmv: M too large");
   const int64_t resident = int64_t(blocks_per_sm) * sm_count();
@@ -323,7 +329,13 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
   sh.stage_bytes = (sh.stage_bytes + 127) / 128 * 128;
   sh.n_blocks = (sh.N + RB - 1) / RB;
   // ring depth: about 96 KB of stages, so that two CTAs fit on an SM
-  sh.stages = std::max(2, std::min(8, (96 * 1024) / sh.stage_bytes));
+  // (QLIN_QMV_RING_KB overrides the target, for tuning)
+  int ring_kb = 96;
+  if (const char* env = std::getenv("QLIN_QMV_RING_KB")) {
+    const int v = std::atoi(env);
+    if (v >= 16 && v <= 200) ring_kb = v;
+  }
+  sh.stages = std::max(2, std::min(8, (ring_kb * 1024) / sh.stage_bytes));
   size_t smem = smem_for(sh, MT, R, BITS);
   while (sh.stages > 2 && smem > 110 * 1024) {
     --sh.stages;
