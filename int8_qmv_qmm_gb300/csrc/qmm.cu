@@ -9,13 +9,17 @@
 // "The blocker (measured)").
 //
 // Orientation ("swap AB"): the MMA's M dimension is 128 weight rows and its N
-// dimension is a tile of BN tokens, so small batches (BN = 16..64) still use
-// the full 128-row MMA and large ones use BN = 128/256.
+// dimension is a tile of BN = 16..256 tokens (the MMA takes about the same
+// time for every N up to 256, so the tile may be wider than the batch; rows
+// past M are zero-filled by the TMA).
 //   D[n][m] (TMEM, f32) += W_hat[n][k] (TMEM, A operand) * x[m][k] (smem, B)
 //
-// Persistent CTAs (one per SM) walk 128 x BN output tiles; the K loop runs in
-// stages of one group (64 k) through a ring of shared-memory stages and, with
-// the same index, of TMEM A slots:
+// Persistent CTAs (one per SM) walk 128 x BN output tiles, or, when the tiles
+// are too few for the SMs, a cluster of 2 or 4 CTAs shares each tile, each
+// CTA taking a slice of K, and the partial accumulators are summed through
+// distributed shared memory at the end.  The K loop runs in stages of one
+// group (64 k) through a ring of shared-memory stages and, with the same
+// index, of TMEM A slots:
 //   warp 0       TMA producer: x tile [BN x 64] (128-byte swizzle), packed
 //                tile [128 rows x 64 codes] (32/64-byte swizzle) and, when the
 //                scale rows are 16-byte aligned, the 8-group scale and bias
@@ -32,9 +36,10 @@
 //                write the row into the stage's A slot with one tcgen05.st.
 //                Keeping A out of shared memory leaves its bandwidth to the
 //                TMA writes and the MMA's reads of x.
-//   warps 10..13 epilogue: tcgen05.ld of their TMEM lane quarter, RNE to the
-//                output type, stores along n; with two accumulators it
-//                overlaps the next tile's K loop.
+//   warps 10..13 epilogue: tcgen05.ld of their TMEM lane quarter, the layer
+//                bias if any (qlin_linear_ex), RNE to the output type (or
+//                float32), stores along n; with two accumulators it overlaps
+//                the next tile's K loop.
 //
 // Every mbarrier wait is bounded (about 2 s); a wait that gives up records a
 // bit in a device status word, the CTA unwinds (waiting, bounded, for its own
