@@ -210,6 +210,12 @@ def max_over_ranks(dist, value: float, device):
     return float(t.item())
 
 
+def replica_throughput(world: int, steps: int, t_max: float) -> float:
+    """Whole-job steps per second: every rank ran `steps` independent steps;
+    the job took as long as its slowest rank."""
+    return world * steps / t_max
+
+
 def barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -280,7 +286,7 @@ def flush_l2(buf):
     buf[: buf.numel() // 2].sum()
 
 
-def time_qmm(q, device, peaks, reps: int = 10, warm: int = 3):
+def time_qmm(q, device, peaks, reps: int = 100, warm: int = 10):
     """Tensor-core qmm on the prefill shapes (M = 512 and 2048), L2 flushed
     between timed launches."""
     import torch
@@ -326,7 +332,7 @@ def time_qmm(q, device, peaks, reps: int = 10, warm: int = 3):
     }
 
 
-def crossover_sweep(q, device, reps: int = 10, warm: int = 3):
+def crossover_sweep(q, device, reps: int = 100, warm: int = 10):
     """qmv vs qmm on the batched-decode sweep (M = 1..32, 4-bit, bf16), L2
     flushed between timed launches; the crossover is the smallest M from which
     qmm is faster on every shape."""
@@ -537,7 +543,7 @@ def bench_ours(args):
         t_local = time_graph_steps(step, args.steps, device, dist)
     t = max_over_ranks(dist, t_local, device)
     per_step = t / args.steps
-    value = world * args.steps / t
+    value = replica_throughput(world, args.steps, t)
 
     # ---- the dominant kernel (qmv) launch by launch, CUDA events on its stream
     alg_list = step.algorithmic_bytes()
