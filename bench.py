@@ -455,6 +455,53 @@ def time_graph_steps(step, steps, device, dist=None):
     return e0.elapsed_time(e1) * 1e-3
 
 
+def qmm_chain_timing(q, device, m: int = 512, layers: int = 4, reps: int = 50):
+    """A prefill-like chain of dependent qmm launches (o 2048x2048, gate
+    8192x2048, down 2048x8192 per layer, 4-bit, M tokens; each output is the
+    next input), in one CUDA graph, plain and with QLIN_OVERLAP_PREVIOUS.
+    The weights (about 40 MB) stay in L2 across replays: this measures the
+    launch overlap, not HBM."""
+    import torch
+
+    from int8_qmv_qmm_gb300 import synthetic as S
+    dims = [(2048, 2048), (8192, 2048), (2048, 8192)] * layers
+    ws = []
+    for i, (n, k) in enumerate(dims):
+        w = torch.from_numpy(S.weights_f32(S.weight_seed(9, i), n, k)).to(device)
+        ws.append(q.quantize_affine(w, 4, sdtype=torch.float16))
+        del w
+    x0 = (S.activations(9, m, 2048, "f16") * 0.05).to(device)
+    outs = [torch.empty((m, n), dtype=torch.float16, device=device) for n, _ in dims]
+    res = {"links": len(dims), "m": m, "note": "L2-warm; 4-bit; o, gate, down per layer"}
+    for overlap in (False, True):
+        def run():
+            x = x0
+            for i, (wq, sc, bi) in enumerate(ws):
+                x = q.qmm(x, wq, sc, bi, 4, out=outs[i], overlap_previous=overlap and i > 0)
+        run()
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(20_000_000)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize(device)
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        flops = sum(2.0 * m * n * k for n, k in dims)
+        res["overlap_us" if overlap else "plain_us"] = us
+        res["overlap_tflops" if overlap else "plain_tflops"] = flops / us / 1e6
+        del g
+    return res
+
+
 def dense_f16_step(q, step, device, steps: int):
     """The same decode step with every weight resident as dense f16 (built
     once with qlin_dequant, outside the timed region) and each linear run as
@@ -579,6 +626,7 @@ def bench_ours(args):
     e2e_value = world * args.steps / t_e2e
 
     qmm_res = None if args.no_qmm else time_qmm(q, device, peaks)
+    qmm_chain = None if args.no_qmm else qmm_chain_timing(q, device)
     cross = None if args.no_qmm else crossover_sweep(q, device)
     status = q.device_status()
 
@@ -616,6 +664,7 @@ def bench_ours(args):
                        "kernel_gbs": alg / chain_s / 1e9},
         "dense_f16_step": dict(dense, packed_speedup=value / world / dense["tokens_per_s"]),
         "qmm": qmm_res,
+        "qmm_chain": qmm_chain,
         "crossover": cross,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x_host.numel() * 2,
                 "d2h_bytes_per_step": logits_host.numel() * 2},

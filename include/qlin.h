@@ -216,6 +216,15 @@ qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, cons
                      void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
                      qlin_dtype dtype, void* stream);
 
+/* qlin_qmm with launch flags (0 = same as qlin_qmm).  QLIN_OVERLAP_PREVIOUS
+ * as for qlin_qmv_ex: the launch and the kernel's set-up (barriers, tensor
+ * memory, descriptor prefetch) overlap the preceding kernel on the stream; x
+ * is read and y written only after that kernel has completed.  Unknown flag
+ * bits return QLIN_ERR_INVALID_ARG. */
+qlin_status qlin_qmm_ex(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                        void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
+                        qlin_dtype dtype, unsigned flags, void* stream);
+
 /*
  * Dispatch to qlin_qmv when M < qlin_crossover_m(N, K, bits), else qlin_qmm.
  */

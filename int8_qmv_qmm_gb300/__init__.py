@@ -47,6 +47,7 @@ _SIGNATURES = {
     "qlin_qmv": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_qmv_ex": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [ctypes.c_uint, _c_vp]),
     "qlin_qmm": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
+    "qlin_qmm_ex": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [ctypes.c_uint, _c_vp]),
     "qlin_linear": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_linear_ex": (_c_int, [_c_vp] * 6 + [_c_i64] * 3 + [_c_int] * 4 + [_c_vp]),
     "qlin_crossover_m": (_c_i64, [_c_i64, _c_i64, _c_int]),
@@ -172,8 +173,15 @@ def qmv(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None, overlap_pr
     return _matmul("qlin_qmv", x, wq, scales, biases, bits, group_size, out)
 
 
-def qmm(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None):
-    """y = x . w_hat^T on the tcgen05 tensor cores (batched decode, prefill)."""
+def qmm(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None, overlap_previous=False):
+    """y = x . w_hat^T on the tcgen05 tensor cores (batched decode, prefill).
+
+    overlap_previous=True launches with QLIN_OVERLAP_PREVIOUS (qlin_qmm_ex):
+    only valid when the preceding work on the stream does not write
+    wq/scales/biases."""
+    if overlap_previous:
+        return _matmul("qlin_qmm_ex", x, wq, scales, biases, bits, group_size, out,
+                       flags=QLIN_OVERLAP_PREVIOUS)
     return _matmul("qlin_qmm", x, wq, scales, biases, bits, group_size, out)
 
 

@@ -175,6 +175,14 @@ qlin_status qlin_qmv_ex(const void* x, const uint32_t* wq, const void* scales, c
                       group_size, dtype, flags, stream);
 }
 
+qlin_status qlin_qmm_ex(const void* x, const uint32_t* wq, const void* scales,
+                        const void* biases, void* y, int64_t M, int64_t N, int64_t K, int bits,
+                        int group_size, qlin_dtype dtype, unsigned flags, void* stream) {
+  g_last_error[0] = 0;
+  return matmul_entry("qlin_qmm_ex", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,
+                      group_size, dtype, flags, stream);
+}
+
 qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
                      qlin_dtype dtype, void* stream) {

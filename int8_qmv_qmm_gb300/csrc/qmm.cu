@@ -313,6 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot_ptr;
+  // programmatic dependent launch (QLIN_OVERLAP_PREVIOUS): the set-up above
+  // ran while the preceding kernel finished; the next kernel may launch now.
+  // Both calls are no-ops in a plain launch.
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -321,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t round = 0;
       uint32_t full_ph = 0;  // bit g*8+s: parity of the next phase of full_bar(g, s)
       bool ok = true;
+      grid_dependency_wait();  // x is the preceding kernel's output
       for (int t = t_first; t < total_tiles && ok; t += t_step) {
         const int n0 = (t % n_tiles) * kBM, m0 = (t / n_tiles) * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -506,6 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int r = quarter * 32 + lane;
     int i = 0;
+    grid_dependency_wait();  // y is written only after the preceding kernel
     for (int t = t_first; t < total_tiles; t += t_step, ++i) {
       const int buf = i % L::kDBufs;
       if (!__all_sync(0xffffffffu,
@@ -740,7 +746,7 @@ qlin_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, 
 template <int BITS, typename AT, int BN>
 qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                       void* y, int64_t M, int64_t N, int64_t K, int split, const Epilogue& ep,
-                      cudaStream_t st) {
+                      unsigned flags, cudaStream_t st) {
   using L = Layout<BITS, BN>;
   constexpr int kMaxSmem = 227 * 1024;
   constexpr int kBarBytes = 512;
@@ -810,13 +816,22 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
   cfg.blockDim = dim3(unsigned(kThreads), 1u, 1u);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(split);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int n_attr = 0;
+  if (split > 1) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = unsigned(split);
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
+  if (flags & QLIN_OVERLAP_PREVIOUS) {
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = split > 1 ? 1 : 0;
+  cfg.numAttrs = n_attr;
   const cudaError_t e = cudaLaunchKernelEx(
       &cfg, kern, tm_x, tm_w, tm_s, tm_b, static_cast<const AT*>(scales),
       static_cast<const AT*>(biases), static_cast<AT*>(y), int(M), int(N), int(K), stages,
@@ -831,7 +846,7 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
 template <int BITS, typename AT>
 qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, int64_t M, int64_t N, int64_t K, const Epilogue& ep,
-                     cudaStream_t st) {
+                     unsigned flags, cudaStream_t st) {
   // Token tile and split-K factor: the pair with the smallest estimated time,
   // waves of tiles x stages per CTA x time per stage, + the reduction when K
   // is split.  Measured on GB300, a stage takes about 0.43 us whatever BN:
@@ -877,11 +892,16 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
     if (v == 1 || v == 2 || v == 4) split = v;
   }
   switch (bn) {
-    case 16: return launch_bn<BITS, AT, 16>(x, wq, scales, biases, y, M, N, K, split, ep, st);
-    case 32: return launch_bn<BITS, AT, 32>(x, wq, scales, biases, y, M, N, K, split, ep, st);
-    case 64: return launch_bn<BITS, AT, 64>(x, wq, scales, biases, y, M, N, K, split, ep, st);
-    case 128: return launch_bn<BITS, AT, 128>(x, wq, scales, biases, y, M, N, K, split, ep, st);
-    default: return launch_bn<BITS, AT, 256>(x, wq, scales, biases, y, M, N, K, split, ep, st);
+    case 16: return launch_bn<BITS, AT, 16>(x, wq, scales, biases, y, M, N, K, split, ep, flags,
+                                               st);
+    case 32: return launch_bn<BITS, AT, 32>(x, wq, scales, biases, y, M, N, K, split, ep, flags,
+                                               st);
+    case 64: return launch_bn<BITS, AT, 64>(x, wq, scales, biases, y, M, N, K, split, ep, flags,
+                                               st);
+    case 128: return launch_bn<BITS, AT, 128>(x, wq, scales, biases, y, M, N, K, split, ep, flags,
+                                               st);
+    default: return launch_bn<BITS, AT, 256>(x, wq, scales, biases, y, M, N, K, split, ep, flags,
+                                              st);
   }
 }
 
@@ -890,12 +910,12 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
 qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
                        unsigned flags, const Epilogue& ep, cudaStream_t st) {
-  (void)flags;
   if (dtype == QLIN_F16)
-    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, ep, st)
-                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, ep, st);
-  return bits == 4 ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, ep, st)
-                   : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, ep, st);
+    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, ep, flags, st)
+                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, ep, flags, st);
+  return bits == 4
+             ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, ep, flags, st)
+             : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, ep, flags, st);
 }
 
 cudaError_t qmm_take_device_status(unsigned* flags) {

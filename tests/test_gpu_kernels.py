@@ -235,6 +235,35 @@ def test_linear_f32_output_is_the_unrounded_sum(dev):
     assert torch.equal(y32.to(torch.float16), y16)
 
 
+@pytest.mark.parametrize("m", [512, 40])
+def test_qmm_overlapped_chain_equals_plain_launches(dev, m):
+    """Dependent qmm launches with QLIN_OVERLAP_PREVIOUS (each reads the
+    previous output) give bit for bit what plain launches give, on the
+    persistent and on the split-K (cluster) path."""
+    dims = [(2048, 2048), (2048, 2048), (8192, 2048), (2048, 8192)]  # (N, K) per link
+    ws = []
+    for i, (n, k) in enumerate(dims):
+        w = torch.from_numpy(S.weights_f32(7000 + i, n, k)).to(dev)
+        ws.append(q.quantize_affine(w, 4, sdtype=torch.float16))
+    x0 = (S.activations(7100 + m, m, 2048, "f16") * 0.05).to(dev)
+
+    def run(overlap):
+        # each link's N is the next link's K: its output is the next input
+        outs, x = [], x0
+        for i, (wq, sc, bi) in enumerate(ws):
+            x = q.qmm(x, wq, sc, bi, 4, overlap_previous=overlap and i > 0)
+            outs.append(x)
+        return outs
+
+    plain = run(False)
+    torch.cuda.synchronize()
+    over = run(True)
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    for a, b in zip(plain, over):
+        assert torch.equal(a, b)
+
+
 def test_empty_batch_is_a_no_op(dev):
     wq = torch.zeros((8, 64), dtype=torch.int32, device=dev)
     sc = torch.zeros((8, 8), dtype=torch.float16, device=dev)
