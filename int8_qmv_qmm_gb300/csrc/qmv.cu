@@ -88,6 +88,10 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m0 = blockIdx.y * MT;
 
+  // the next kernel may launch at once: it only streams its own (read-only)
+  // weights before its own dependency wait, which this kernel's completion
+  // releases (0.3% faster on the decode step than triggering after the wait)
+  grid_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < sh.stages; ++s) {
       ptx::mbar_init(full0 + 8u * s, 1);
@@ -167,9 +171,8 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
 
   // --------------------------------------------------------------- consumers
   // x is produced by the preceding kernel: wait for it (a no-op unless this is
-  // a programmatic dependent launch), then let the next kernel launch early.
+  // a programmatic dependent launch).
   grid_dependency_wait();
-  grid_launch_dependents();
   stage_x<BITS, MT, AT, false>(x + int64_t(m0) * K, K, sh.M - m0, K, sh.rounds, xs, xsum, tid);
 
   const StageGeom geom{sh.kt_bytes, kt_groups, sh.rounds, gpr, N};
