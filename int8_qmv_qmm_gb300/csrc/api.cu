@@ -7,6 +7,7 @@
 #include <cstring>
 
 #include "qlin_internal.h"
+#include "qlin_testing.h"
 
 namespace qlin {
 
@@ -196,10 +197,13 @@ size_t qlin_qmv_chain_workspace_size(int n_links) {
   return (size_t(n_links) * sizeof(unsigned) + 255) / 256 * 256;
 }
 
-qlin_status qlin_qmv_chain(const void* x0, const qlin_link* links, int n_links, int bits,
-                           int group_size, qlin_dtype dtype, void* workspace,
-                           size_t workspace_bytes, void* stream) {
-  g_last_error[0] = 0;
+}  // extern "C"
+
+namespace qlin {
+namespace {
+qlin_status chain_entry(const void* x0, const qlin_link* links, int n_links, int bits,
+                        int group_size, qlin_dtype dtype, void* workspace, size_t workspace_bytes,
+                        const ChainWaitOptions& wo, void* stream) {
   if (!links || n_links < 1 || n_links > chain_max_links())
     return fail(QLIN_ERR_INVALID_ARG, "qlin_qmv_chain: need 1..%d links", chain_max_links());
   qlin_status s = check_act_dtype(dtype, "activation/scale");
@@ -238,17 +242,55 @@ qlin_status qlin_qmv_chain(const void* x0, const qlin_link* links, int n_links, 
                     "qlin_qmv_chain: link %d's input must start 16-byte aligned", l);
     }
   }
-  return launch_qmv_chain(x0, links, n_links, bits, dtype, workspace,
+  return launch_qmv_chain(x0, links, n_links, bits, dtype, workspace, wo,
                           reinterpret_cast<cudaStream_t>(stream));
+}
+}  // namespace
+}  // namespace qlin
+
+extern "C" {
+
+qlin_status qlin_qmv_chain(const void* x0, const qlin_link* links, int n_links, int bits,
+                           int group_size, qlin_dtype dtype, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  g_last_error[0] = 0;
+  return chain_entry(x0, links, n_links, bits, group_size, dtype, workspace, workspace_bytes,
+                     kDefaultChainWaits, stream);
+}
+
+qlin_status qlin_testing_qmv_chain_stalled(const void* x0, const qlin_link* links, int n_links,
+                                           int bits, int group_size, qlin_dtype dtype,
+                                           void* workspace, size_t workspace_bytes,
+                                           int stalled_link, unsigned wait_limit_us,
+                                           void* stream) {
+  g_last_error[0] = 0;
+  if (!links || n_links < 1 || stalled_link < 0 || stalled_link >= n_links)
+    return fail(QLIN_ERR_INVALID_ARG, "qlin_testing_qmv_chain_stalled: stalled_link %d",
+                stalled_link);
+  bool read = false;
+  for (int l = stalled_link + 1; l < n_links; ++l) read = read || links[l].input == stalled_link;
+  if (!read)
+    return fail(QLIN_ERR_INVALID_ARG,
+                "qlin_testing_qmv_chain_stalled: no link reads link %d, nothing would wait",
+                stalled_link);
+  if (wait_limit_us < 1 || wait_limit_us > 2000000u)
+    return fail(QLIN_ERR_INVALID_ARG, "qlin_testing_qmv_chain_stalled: wait_limit_us %u",
+                wait_limit_us);
+  const ChainWaitOptions wo = {1000ull * wait_limit_us, stalled_link};
+  return chain_entry(x0, links, n_links, bits, group_size, dtype, workspace, workspace_bytes, wo,
+                     stream);
 }
 
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
   (void)bits;
-  const char* env = getenv("QLIN_CROSSOVER_M");
-  if (env && *env) {
-    long long v = atoll(env);
-    if (v >= 1) return v;
-  }
+  // QLIN_CROSSOVER_M (a positive integer) overrides the measured choice; read
+  // once, on the first call
+  static const long long env_m = [] {
+    const char* env = getenv("QLIN_CROSSOVER_M");
+    const long long v = env && *env ? atoll(env) : 0;
+    return v >= 1 ? v : 0;
+  }();
+  if (env_m) return env_m;
   // Measured on GB300 (batched-decode sweep, 4-bit, bf16, L2 flushed): the
   // tensor-core kernel (wide token tiles, K split over a cluster) overtakes
   // the CUDA-core one at M = 8 when N >= K (8192 x 2048: 16.4 vs 20.5 us) and

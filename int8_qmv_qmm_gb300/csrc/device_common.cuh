@@ -36,14 +36,6 @@ struct Act<__nv_bfloat16> {
 
 __device__ __forceinline__ float u32_as_f32(uint32_t v) { return __uint_as_float(v); }
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 // Asks L2 to fetch [p, p + bytes) (p and bytes multiples of 16); no data
 // comes back to the SM.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {

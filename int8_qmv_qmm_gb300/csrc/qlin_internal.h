@@ -38,8 +38,18 @@ qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, co
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
                        unsigned flags, const Epilogue& ep, cudaStream_t st);
 
+// Limits of the chain kernel's waits for an input link.  stalled_link >= 0
+// (tests only) makes the readers of that link wait for one row block more
+// than it has, so that their wait runs out.
+struct ChainWaitOptions {
+  unsigned long long dep_wait_ns;
+  int stalled_link;
+};
+constexpr ChainWaitOptions kDefaultChainWaits = {2000000000ull, -1};
+
 qlin_status launch_qmv_chain(const void* x0, const qlin_link* links, int n_links, int bits,
-                             qlin_dtype dtype, void* ws, cudaStream_t st);
+                             qlin_dtype dtype, void* ws, const ChainWaitOptions& wo,
+                             cudaStream_t st);
 int chain_max_links();
 
 // Read and clear the kernels' device status words (no synchronisation).

@@ -36,6 +36,14 @@
 //                write the row into the stage's A slot with one tcgen05.st.
 //                Keeping A out of shared memory leaves its bandwidth to the
 //                TMA writes and the MMA's reads of x.
+//                bfloat16 keeps only 8 significant bits, so rounding w_hat to
+//                it moves a weight by up to 2^-8 of its value, as much as the
+//                whole output tolerance.  For bfloat16 the A slot therefore
+//                holds two operands, hi = RNE(w_hat) (the reconstruction
+//                itself) and a residual lo, and each K step issues two MMAs
+//                into the same accumulator: hi + lo is w_hat to about 2^-15,
+//                and rounding hi + lo to bfloat16 gives back hi exactly.
+//                float16 (11 bits) needs no residual.
 //   warps 10..13 epilogue: tcgen05.ld of their TMEM lane quarter, the layer
 //                bias if any (qlin_linear_ex), RNE to the output type (or
 //                float32), stores along n; with two accumulators it overlaps
@@ -121,10 +129,18 @@ struct Geo {
 
 __host__ __device__ constexpr int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
+// Operands per weight in the A slot: 1 (float16: w_hat), 2 (bfloat16: hi and
+// the residual lo, see lo_pair).
+template <typename AT>
+struct OperandSplit {
+  static constexpr int value = std::is_same<AT, __nv_bfloat16>::value ? 2 : 1;
+};
+
 // Shared-memory stage: [x tile][packed tile][8 groups of scales, of biases].
-// TMEM: kDBufs accumulators of BN columns, then one 32-column slot per ring
-// stage holding the stage's dequantised A tile (128 lanes x 64 16-bit values).
-template <int BITS, int BN>
+// TMEM: kDBufs accumulators of BN columns, then one slot of SPLIT x 32 columns
+// per ring stage holding the stage's dequantised A tile(s) (128 lanes x 64
+// 16-bit values each).
+template <int BITS, int BN, int SPLIT>
 struct Layout {
   static constexpr int kXBytes = BN * kBK * 2;           // x tile, 128-byte rows
   static constexpr int kWBytes = Geo<BITS>::kPackedBytes;
@@ -137,7 +153,7 @@ struct Layout {
   // unless they would leave TMEM too few A slots
   static constexpr int kDBufs = BN >= 256 ? 1 : 2;
   static constexpr int kACol0 = kDBufs * BN < 32 ? 32 : kDBufs * BN;
-  static constexpr int kAColsPerStage = kBK / 2;         // 64 16-bit values per lane
+  static constexpr int kAColsPerStage = SPLIT * kBK / 2;  // 64 16-bit values per lane each
   static constexpr int kMaxStages = (512 - kACol0) / kAColsPerStage;
 };
 
@@ -202,6 +218,68 @@ __device__ __forceinline__ void dequant_word8<__nv_bfloat16>(uint32_t w, uint32_
   p1 = *reinterpret_cast<const uint32_t*>(&r1);
 }
 
+// ---- bfloat16 residual operand
+// For a pair of weights with codes q (exact, as float), scale s and bias b in
+// float32, and hi = RNE_bf16(q*s + b) (the pair as computed above):
+//   d  = RNE_f32(q*s + b) - hi          (exact: the two are within 2^-8)
+//   lo = RZ_bf16(RNE_f32(d * (1 - 2^-9)))
+// Then |hi + lo - (q*s + b)| <= about 2^-15 |q*s + b|, and |lo| stays below
+// half a bfloat16 step of hi (the factor keeps it there when the float32
+// rounding lands exactly on a midpoint), so hi + lo, accumulated in float32
+// and rounded to bfloat16, is hi again: a one-hot x still reproduces the
+// reconstruction bit for bit.
+__device__ __forceinline__ uint32_t lo_pair(float2 q, float2 s, float2 b, uint32_t hi) {
+  const float2 fw = __ffma2_rn(q, s, b);
+  const float2 h = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+  const float2 d = __ffma2_rn(h, make_float2(-1.0f, -1.0f), fw);
+  const float2 dc = __fmul2_rn(d, make_float2(0.998046875f, 0.998046875f));
+  uint32_t r;
+  // the first source goes to the upper half
+  asm("cvt.rz.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(dc.y), "f"(dc.x));
+  return r;
+}
+
+// 8 codes of a 4-bit word -> hi and lo of 8 bfloat16 weights.
+__device__ __forceinline__ void dequant_word4_split(uint32_t w, uint32_t s2, uint32_t b2, float2 sf,
+                                                    float2 bf, uint32_t (&hi)[4],
+                                                    uint32_t (&lo)[4]) {
+  const uint32_t sh = w >> 4;
+  const uint32_t mq = Act<__nv_bfloat16>::kMagic2;
+  const __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162*>(&mq);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t sel = uint32_t(j) | (uint32_t(j) << 4) | (uint32_t(4 + j) << 8) |
+                         (uint32_t(4 + j) << 12);
+    const uint32_t mp = (__byte_perm(w, sh, sel) & 0x000F000Fu) | Act<__nv_bfloat16>::kMagic2;
+    const __nv_bfloat162 q = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&mp), m);
+    const __nv_bfloat162 r = __hfma2(q, *reinterpret_cast<const __nv_bfloat162*>(&s2),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&b2));
+    const uint32_t qb = *reinterpret_cast<const uint32_t*>(&q);
+    hi[j] = *reinterpret_cast<const uint32_t*>(&r);
+    lo[j] = lo_pair(make_float2(__uint_as_float(qb << 16), __uint_as_float(qb & 0xffff0000u)), sf,
+                    bf, hi[j]);
+  }
+}
+
+// 4 codes of an 8-bit word -> hi and lo of 4 bfloat16 weights (two pairs).
+__device__ __forceinline__ void dequant_word8_split(uint32_t w, uint32_t s2, uint32_t b2, float2 sf,
+                                                    float2 bf, uint32_t& h0, uint32_t& h1,
+                                                    uint32_t& l0, uint32_t& l1) {
+  float f[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    f[i] = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | uint32_t(i))) - 8388608.0f;
+  const __nv_bfloat162 q01 = __floats2bfloat162_rn(f[0], f[1]);
+  const __nv_bfloat162 q23 = __floats2bfloat162_rn(f[2], f[3]);
+  const __nv_bfloat162 s = *reinterpret_cast<const __nv_bfloat162*>(&s2);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&b2);
+  const __nv_bfloat162 r0 = __hfma2(q01, s, b), r1 = __hfma2(q23, s, b);
+  h0 = *reinterpret_cast<const uint32_t*>(&r0);
+  h1 = *reinterpret_cast<const uint32_t*>(&r1);
+  l0 = lo_pair(make_float2(f[0], f[1]), sf, bf, h0);
+  l1 = lo_pair(make_float2(f[2], f[3]), sf, bf, h1);
+}
+
 // ---- thread-block cluster helpers (split-K reduction)
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -249,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                const AT* __restrict__ scales, const AT* __restrict__ biases, AT* __restrict__ y,
                int M, int N, int K, int stages, int tmem_cols, int split,
                const AT* __restrict__ layer_bias, int y_f32) {
-  using L = Layout<BITS, BN>;
+  constexpr int kSplit = OperandSplit<AT>::value;
+  using L = Layout<BITS, BN, kSplit>;
   using G = Geo<BITS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
@@ -399,6 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // +2 in the descriptor's 16-byte address units
             mma_f16_ts(d_tmem, a_tmem + uint32_t(8 * kk), bd + uint64_t(2 * kk), idesc,
                        (kb > kb0 || kk > 0) ? 1u : 0u);
+            if constexpr (kSplit == 2)  // the bfloat16 residual lo, 32 columns on
+              mma_f16_ts(d_tmem, a_tmem + uint32_t(32 + 8 * kk), bd + uint64_t(2 * kk), idesc, 1u);
           }
           any = true;
           ptx::mma_commit(empty_bar(s));
@@ -460,8 +541,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s2 = row_ok ? splat(sc) : 0u, b2 = row_ok ? splat(bc) : 0u;
         const uint8_t* wrow = gbase + (w_addr(cs) - base) + r * G::kPackedRowBytes;
         // the row's 64 reconstructed weights, two per register, k ascending
+        // (and, for bfloat16, their residuals)
         uint32_t a[32];
-        if constexpr (BITS == 4) {
+        uint32_t lo[kSplit == 2 ? 32 : 1];
+        if constexpr (kSplit == 2) {
+          const float sv = row_ok ? Act<AT>::to_f32(sc) : 0.0f;
+          const float bv = row_ok ? Act<AT>::to_f32(bc) : 0.0f;
+          const float2 sf = make_float2(sv, sv), bf = make_float2(bv, bv);
+          if constexpr (BITS == 4) {
+            const int sw = (r >> 2) & 1;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(wrow + ((0 ^ sw) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
+            const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              dequant_word4_split(words[c], s2, b2, sf, bf,
+                                  *reinterpret_cast<uint32_t(*)[4]>(a + 4 * c),
+                                  *reinterpret_cast<uint32_t(*)[4]>(lo + 4 * c));
+          } else {
+            const int sw = (r >> 1) & 3;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ sw) << 4));
+              const uint32_t ws4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dequant_word8_split(ws4[e], s2, b2, sf, bf, a[8 * c + 2 * e], a[8 * c + 2 * e + 1],
+                                    lo[8 * c + 2 * e], lo[8 * c + 2 * e + 1]);
+            }
+          }
+        } else if constexpr (BITS == 4) {
           // packed rows are 32 bytes in the 32-byte TMA swizzle: chunk c of row
           // r sits at chunk c ^ ((r >> 2) & 1)
           const int sw = (r >> 2) & 1;
@@ -497,6 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // into the stage's A slot; complete before the MMA issuer is told
         tmem_st_32x32b_x32(a_lane + uint32_t(cs * L::kAColsPerStage), a);
+        if constexpr (kSplit == 2)
+          tmem_st_32x32b_x32(a_lane + uint32_t(cs * L::kAColsPerStage + 32), lo);
         tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
@@ -747,7 +858,7 @@ template <int BITS, typename AT, int BN>
 qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                       void* y, int64_t M, int64_t N, int64_t K, int split, const Epilogue& ep,
                       unsigned flags, cudaStream_t st) {
-  using L = Layout<BITS, BN>;
+  using L = Layout<BITS, BN, OperandSplit<AT>::value>;
   constexpr int kMaxSmem = 227 * 1024;
   constexpr int kBarBytes = 512;
   // (kDequantGroups + 2) barriers per stage (at most 8), two pairs of
@@ -867,7 +978,8 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
   double best = -1.0;
   for (int cand = max_bn; cand >= 16; cand >>= 1) {
     const int64_t tiles = n_tiles * ((M + cand - 1) / cand);
-    const double t_stage = 0.43;
+    // (bfloat16 issues twice the MMAs per stage: the residual operand)
+    const double t_stage = OperandSplit<AT>::value == 2 ? 0.75 : 0.43;
     for (int sp = 1; sp <= 4; sp *= 2) {
       if (sp > 1 && (tiles * sp > sms || kb_count < 4 * sp || cand / sp < 16)) continue;
       const int64_t waves = (tiles * sp + sms - 1) / sms;

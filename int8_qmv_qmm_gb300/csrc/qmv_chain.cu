@@ -65,10 +65,12 @@ struct LinkDev {
 struct ChainParams {
   LinkDev links[kMaxLinks];
   unsigned* counters;
+  unsigned long long dep_wait_ns;  // limit of one wait for an input link
   int n_links;
   int stages;
   int stage_bytes;
-  int rounds_max;  // x layout rounds of the longest K
+  int rounds_max;    // x layout rounds of the longest K
+  int stalled_link;  // tests only: readers of this link wait for one block too many (-1: none)
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -179,28 +181,32 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_chain_kernel(const __grid_con
 
   // --------------------------------------------------------------- consumers
   // Control flow here is the same on every consumer thread whatever happens:
-  // a wait that gives up records the failure and later waits are skipped, so
-  // the named CTA barriers below are always reached by all 256 threads (the
-  // results are then garbage and the status word says so).
+  // a wait that gives up records the failure, so the named CTA barriers below
+  // are always reached by all 256 threads (the results are then garbage and
+  // the status word says so).  A dependency wait that gives up only skips the
+  // later dependency waits: the ring waits go on, so every bulk copy the
+  // producer issued has landed before the CTA exits.  A ring wait that gives
+  // up skips the later ring waits (each would take the full limit).
   int s = 0;
   uint32_t round = 0;
-  bool ok = true;
+  bool dep_ok = true, ring_ok = true;
   float2* sbw = sb32 + warp * kR * 32;
   for (int l = 0; l < p.n_links; ++l) {
     const LinkDev& L = p.links[l];
     const int j0 = first_block(L, c, G);
     if (j0 >= L.n_blocks) continue;  // this CTA owns no block of this link
     if (L.dep >= 0) {
-      if (tid == 0 && ok) {
-        const unsigned target = unsigned(p.links[L.dep].n_blocks);
+      if (tid == 0 && dep_ok) {
+        const unsigned target =
+            unsigned(p.links[L.dep].n_blocks) + (L.dep == p.stalled_link ? 1u : 0u);
         const unsigned* ctr = p.counters + L.dep;
         if (ld_acquire(ctr) < target) {
           const uint64_t t0 = ptx::globaltimer_ns();
           for (uint32_t i = 1;; ++i) {
             if (ld_acquire(ctr) >= target) break;
-            if ((i & 255u) == 0 && ptx::globaltimer_ns() - t0 > 2000000000ull) {
+            if ((i & 255u) == 0 && ptx::globaltimer_ns() - t0 > p.dep_wait_ns) {
               atomicOr(&g_chain_status, 4u);
-              ok = false;
+              dep_ok = false;
               break;
             }
           }
@@ -221,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_chain_kernel(const __grid_con
 #pragma unroll
       for (int r = 0; r < kR; ++r) acc[r][0] = make_float2(0.0f, 0.0f);
       for (int kt = 0; kt < L.n_kt; ++kt) {
-        if (ok && !ptx::mbar_wait(full0 + 8u * s, round & 1u)) {
+        if (ring_ok && !ptx::mbar_wait(full0 + 8u * s, round & 1u)) {
           if (lane == 0) atomicOr(&g_chain_status, 2u);
-          ok = false;
+          ring_ok = false;
         }
         const uint8_t* stage = ring + size_t(s) * p.stage_bytes;
         if (L.fast) {
@@ -253,11 +259,13 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_chain_kernel(const __grid_con
 // ------------------------------------------------------------------- host
 template <int BITS, typename AT>
 qlin_status launch_chain_t(const void* x0, const qlin_link* links, int n_links, void* ws,
-                           cudaStream_t st) {
+                           const ChainWaitOptions& wo, cudaStream_t st) {
   auto kern = qmv_chain_kernel<BITS, AT>;
   ChainParams p;  // ~13 KB, passed by value as the kernel's parameter block
   p.n_links = n_links;
   p.counters = static_cast<unsigned*>(ws);
+  p.dep_wait_ns = wo.dep_wait_ns;
+  p.stalled_link = wo.stalled_link;
   int max_kt_bytes = 0, max_k = 0, max_groups = 0;
   for (int l = 0; l < n_links; ++l) {
     const qlin_link& in = links[l];
@@ -350,12 +358,13 @@ qlin_status launch_chain_t(const void* x0, const qlin_link* links, int n_links, 
 int chain_max_links() { return kMaxLinks; }
 
 qlin_status launch_qmv_chain(const void* x0, const qlin_link* links, int n_links, int bits,
-                             qlin_dtype dtype, void* ws, cudaStream_t st) {
+                             qlin_dtype dtype, void* ws, const ChainWaitOptions& wo,
+                             cudaStream_t st) {
   if (dtype == QLIN_F16)
-    return bits == 4 ? launch_chain_t<4, __half>(x0, links, n_links, ws, st)
-                     : launch_chain_t<8, __half>(x0, links, n_links, ws, st);
-  return bits == 4 ? launch_chain_t<4, __nv_bfloat16>(x0, links, n_links, ws, st)
-                   : launch_chain_t<8, __nv_bfloat16>(x0, links, n_links, ws, st);
+    return bits == 4 ? launch_chain_t<4, __half>(x0, links, n_links, ws, wo, st)
+                     : launch_chain_t<8, __half>(x0, links, n_links, ws, wo, st);
+  return bits == 4 ? launch_chain_t<4, __nv_bfloat16>(x0, links, n_links, ws, wo, st)
+                   : launch_chain_t<8, __nv_bfloat16>(x0, links, n_links, ws, wo, st);
 }
 
 cudaError_t chain_take_device_status(unsigned* flags) {

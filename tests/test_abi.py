@@ -11,8 +11,8 @@ import pytest
 import int8_qmv_qmm_gb300 as q
 from int8_qmv_qmm_gb300 import build_lib
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
-                      "qlin.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADERS = sorted(os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h"))
 OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
 
 
@@ -23,7 +23,7 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(qlin_[a-z_]+)\s*\(", text)))
 
@@ -125,8 +125,34 @@ def test_device_status_rejects_null(L):
     assert L.qlin_device_status(None) == INVALID
 
 
-def test_crossover_env_override(L, monkeypatch):
-    base = L.qlin_crossover_m(8192, 2048, 4)
-    assert base >= 1
-    monkeypatch.setenv("QLIN_CROSSOVER_M", "7")
-    assert L.qlin_crossover_m(8192, 2048, 4) == 7
+def test_crossover_env_override(L):
+    """QLIN_CROSSOVER_M is read once per process (on the first call), so the
+    override is checked in a fresh process."""
+    import subprocess
+    import sys
+    assert L.qlin_crossover_m(8192, 2048, 4) >= 1
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import int8_qmv_qmm_gb300 as q; "
+            "print(q.lib().qlin_crossover_m(8192, 2048, 4))")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                         env=dict(os.environ, QLIN_CROSSOVER_M="7"), timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip().splitlines()[-1] == "7"
+
+
+def test_testing_chain_entry_validation(L):
+    """The test-only stalled-chain entry point refuses bad requests on the host."""
+    vp = ctypes.c_void_p
+    links = (q.Link * 2)()
+    links[0] = q.Link(FAKE, FAKE, FAKE, FAKE, 64, 512, -1, 0)
+    links[1] = q.Link(FAKE, FAKE, FAKE, FAKE, 64, 64, 0, 0)
+
+    def call(stalled, limit_us, n=2):
+        return L.qlin_testing_qmv_chain_stalled(vp(FAKE), links, n, 4, 64, q.QLIN_F16, vp(FAKE),
+                                                256, stalled, limit_us, None)
+
+    assert call(-1, 1000) == INVALID      # out of range
+    assert call(2, 1000) == INVALID
+    assert call(1, 1000) == INVALID       # nothing reads the last link
+    assert call(0, 0) == INVALID          # limit out of range
+    assert call(0, 3000000) == INVALID

@@ -433,3 +433,20 @@ def test_mutations_are_caught():
     assert check_dequant_exact(_dequant_wrong_group_index)
     assert check_matmul_bruteforce(_matmul_transposed_w)
     assert check_matmul_bruteforce(_matmul_dropped_tail)
+
+
+def test_bf16_output_rounding_alone_can_exceed_the_bound():
+    """Why same-sign bf16 cases are checked through the float32 output: with
+    x and w_hat all positive, |y| = sum |x w_hat|, and rounding y to bfloat16
+    (8 significant bits) moves it by up to 2^-8 |y| = 3.9e-3 |y|.  Even the
+    exact product rounded once breaks 2e-3 * sum|x w_hat| + 1e-5 on many
+    outputs, while the float16 rounding (2^-11 |y|) never does."""
+    rng = np.random.default_rng(5)
+    w = np.abs(rng.standard_normal((512, 128)) * 0.02).astype(np.float32)
+    x = np.abs(rng.standard_normal((16, 128))).astype(np.float32)
+    for dt, expect_fail in (("bf16", True), ("f16", False)):
+        xr = O.round_to_format(x.astype(np.float64), dt)
+        ref = O.linear_ref(xr, w, 4, 64, dt)
+        best = O.round_to_format(ref["y_ref"], dt)
+        ok = O.within_tolerance(best, ref["y_ref"], ref["a_ref"])
+        assert (not ok.all()) == expect_fail, dt
