@@ -51,8 +51,7 @@ WORKLOAD = ("llama-3.2-1b-shaped decode step: 16 x (q 2048x2048, k 512x2048, v 5
             "earlier launch's output; launches overlapped with programmatic dependent launch; "
             "one CUDA graph")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-ORACLE_SAMPLE_STRIDE = 4   # cpu_baseline: every 4th output row of every linear (~25%)
-REFERENCE_STRIDE = 256     # reference arm: every 256th row per step (~0.4%)
+DEFAULT_PREFETCH_MB = 0   # L2 prefetch distance of the decode step (measured best)
 
 
 # ------------------------------------------------------------------- helpers
@@ -222,59 +221,160 @@ def barrier(dist):
 
 
 # ---------------------------------------------------------- CPU oracle leg
-def oracle_sample_child(stride: int, steps: int) -> dict:
-    """Runs in a child process with one BLAS thread: times the oracle's
-    per-token work (unpack + exact dequant + f64 matmul) over every
-    `stride`-th output row of every linear of the decode step, `steps` times.
-    Weight generation and quantisation (load-time work) are not timed."""
+# The oracle's per-token work for the decode step (unpack, exact dequant in
+# float64, float64 matmul) on the host cores.  The rows of every linear are
+# cut into the generator's 1024-row blocks, dealt to N worker processes
+# (spawned, one BLAS thread each) so that each holds about the same number of
+# weights; a step sends every worker "go" and ends when the last one is done.
+# Generating and quantising the weights (load-time work) is not timed.
+
+def _step_shapes():
+    from int8_qmv_qmm_gb300 import synthetic as S
+    shapes = [(n, k) for _ in range(S.LLAMA_1B_LAYERS) for (_, n, k) in S.LLAMA_1B_LINEARS]
+    shapes.append(S.LLAMA_1B_LM_HEAD[1:])
+    return shapes
+
+
+def oracle_partition(n_workers: int, block: int = 1024):
+    """Work units (linear index, N, K, first row, end row) per worker:
+    row blocks, largest first, each to the least-loaded worker."""
+    units = []
+    for idx, (n, k) in enumerate(_step_shapes()):
+        for r0 in range(0, n, block):
+            units.append((idx, n, k, r0, min(n, r0 + block)))
+    units.sort(key=lambda u: -(u[4] - u[3]) * u[2])
+    load = [0] * n_workers
+    parts = [[] for _ in range(n_workers)]
+    for u in units:
+        w = min(range(n_workers), key=lambda i: load[i])
+        parts[w].append(u)
+        load[w] += (u[4] - u[3]) * u[2]
+    return parts
+
+
+def _oracle_worker(conn, units, stride):
+    """Worker process: prepares its rows (every `stride`-th row of each unit),
+    then, per message `skip` (0 ends), runs one pass of the per-token work over
+    every `skip`-th prepared unit and sends back (seconds, weights done)."""
     import numpy as np
 
     from int8_qmv_qmm_gb300 import synthetic as S
     from oracle import qlin_oracle as O
-
-    shapes = [(n, k) for _ in range(S.LLAMA_1B_LAYERS) for (_, n, k) in S.LLAMA_1B_LINEARS]
-    shapes.append(S.LLAMA_1B_LM_HEAD[1:])
     prepared = []
-    for idx, (n, k) in enumerate(shapes):
-        rows = np.arange(0, n, stride)
-        w = S.weights_f32(S.weight_seed(2, idx), n, k, rows=rows)
+    for idx, n, k, r0, r1 in units:
+        rows = np.arange(r0, r1)
+        rows = rows[rows % stride == 0]
+        if rows.size == 0:
+            continue
+        w = S.weights_f32(S.weight_seed(2, idx), n, k, rows=rows, threads=1)
         codes, scale, bias = O.quantize_affine(w, 8, 64, "f16")
-        words = O.pack(codes, 8)
         x = S.activations(S.weight_seed(2, idx), 1, k, "f16").float().numpy()
-        prepared.append((words, scale, bias, x, k))
-    sampled = sum(p[0].shape[0] * p[4] for p in prepared)
-    total = sum(n * k for n, k in shapes)
-    times = []
-    for _ in range(steps):
+        prepared.append((O.pack(codes, 8), scale, bias, x, k, rows.size))
+    conn.send(True)
+    while True:
+        skip = conn.recv()
+        if not skip:
+            break
         t0 = time.perf_counter()
-        for words, scale, bias, x, k in prepared:
+        done = 0
+        for words, scale, bias, x, k, nrows in prepared[::skip]:
             codes = O.unpack(words, 8, k)
             w_hat = O.dequant_exact(codes, scale, bias, 64)
             O.matmul_ref(x, w_hat)
-        times.append(time.perf_counter() - t0)
-    return {"times": times, "fraction": sampled / total}
+            done += nrows * k
+        conn.send((time.perf_counter() - t0, done))
+    conn.close()
 
 
-def run_oracle(stride: int, steps: int) -> dict:
+def oracle_steps_child(n_workers: int, stride: int, warmup: int, steps: int,
+                       budget_s: int) -> dict:
+    """Runs in a child process without a GPU: starts the workers, runs one
+    whole pass over the prepared rows as the first warm-up, and, if whole
+    passes would not fit `warmup - 1 + steps` times into `budget_s` seconds,
+    makes each further pass cover every `skip`-th row block only.  Returns the
+    timed passes and the share of the step's weights each covered."""
+    import math
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    parts = oracle_partition(n_workers)
+    procs, conns = [], []
+    for part in parts:
+        a, b = ctx.Pipe()
+        pr = ctx.Process(target=_oracle_worker, args=(b, part, stride), daemon=True)
+        pr.start()
+        procs.append(pr)
+        conns.append(a)
+    for c in conns:
+        c.recv()
+
+    def one_pass(skip):
+        t0 = time.perf_counter()
+        for c in conns:
+            c.send(skip)
+        done = sum(c.recv()[1] for c in conns)
+        return time.perf_counter() - t0, done
+
+    skip = 1
+    t_first, _ = one_pass(1)
+    if t_first * (max(warmup - 1, 0) + steps) > budget_s:
+        skip = math.ceil(t_first * (max(warmup - 1, 0) + steps) / budget_s)
+    for _ in range(max(warmup - 1, 0)):
+        one_pass(skip)
+    times, done = [], 0
+    for _ in range(steps):
+        t, done = one_pass(skip)
+        times.append(t)
+    for c in conns:
+        c.send(0)
+    for pr in procs:
+        pr.join(timeout=60)
+    total = sum(n * k for n, k in _step_shapes())
+    return {"times": times, "fraction": done / total, "workers": n_workers, "skip": skip,
+            "row_stride": stride, "first_pass_s": t_first}
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_oracle(n_workers: int, stride: int, warmup: int, steps: int, budget_s: int) -> dict:
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
                MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child",
-                        str(stride), str(steps)], env=env, stdout=subprocess.PIPE,
-                       stderr=subprocess.PIPE, text=True, timeout=3600)
+                        str(n_workers), str(stride), str(warmup), str(steps), str(budget_s)],
+                       env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
+                       timeout=3600)
     if r.returncode != 0:
         raise RuntimeError(f"oracle child failed: {r.stderr[-2000:]}")
     res = json.loads(r.stdout.strip().splitlines()[-1])
     frac, times = res["fraction"], res["times"]
-    return {"value": len(times) * frac / sum(times), "fraction": frac, "times": times,
-            "sample": (f"every {stride}th output row of all 113 linears of the decode step "
-                       f"({frac * 100:.2f}% of the weights): unpack + exact dequant + f64 "
-                       f"matmul, {sum(times) / len(times):.2f} s per pass, one BLAS thread")}
+    per_pass = sum(times) / len(times)
+    if frac >= 0.999999:
+        what = "whole decode steps (all 113 linears, every output row)"
+    else:
+        what = (f"{frac * 100:.2f}% of the decode step's weights per pass (every "
+                f"{res['row_stride']}th row, every {res['skip']}th block of 1024 rows; a whole "
+                f"step took {res['first_pass_s']:.2f} s); tokens/s-eq extrapolated from that share")
+    return {"value": frac / per_pass, "fraction": frac, "times": times, "s_per_pass": per_pass,
+            "extrapolated": frac < 0.999999,
+            "sample": (f"{what}: unpack + exact dequant + f64 matmul, rows dealt to "
+                       f"{n_workers} worker process(es) with one BLAS thread each, "
+                       f"{len(times)} timed pass(es) of {per_pass:.2f} s")}
 
 
-def run_oracle_baseline(stride: int = ORACLE_SAMPLE_STRIDE) -> dict:
-    r = run_oracle(stride, 4)
-    return {"value": r["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": r["sample"]}
+def run_oracle_baseline() -> dict:
+    """cpu_baseline: two whole decode steps on every host core, and beside it
+    one core on every 16th row (extrapolated)."""
+    cores = host_cores()
+    r = run_oracle(cores, 1, 1, 2, budget_s=30)
+    one = run_oracle(1, 16, 1, 1, budget_s=10)
+    return {"value": r["value"], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": r["sample"],
+            "one_core": {"value": one["value"], "unit": UNIT, "cores": 1,
+                         "sample": one["sample"]}}
 
 
 # ------------------------------------------------------------- GPU legs
@@ -376,8 +476,79 @@ def crossover_sweep(q, device, reps: int = 100, warm: int = 10):
     return {"crossover_m": cross, "table": table}
 
 
+def time_flushed(fn, device, flush, reps: int = 100, warm: int = 10):
+    """Median GPU time of fn() (one or more launches on the current stream),
+    L2 flushed before each timed repetition, host enqueue hidden behind a GPU
+    sleep."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush_l2(flush)
+        torch.cuda._sleep(100000)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    return statistics.median(ts)
+
+
+def small_workloads(q, device, peaks, prefetch_distance):
+    """The two M = 1 workloads below the L2 size, L2 flushed between timed
+    repetitions: the single 300 x 512 qmv (4-bit) and one Llama-3.2-1B
+    decoder layer's seven linears (4-bit), the latter both as the decode
+    step runs them (q/k/v and gate/up fused, 4 overlapped launches in one CUDA
+    graph) and as seven separate launches."""
+    import torch
+
+    from int8_qmv_qmm_gb300 import synthetic as S
+    from int8_qmv_qmm_gb300.decode_step import DecodeStep
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+    out = {}
+    # single qmv: M = 1, K = 512, N = 300 (N not a multiple of 4)
+    w = torch.from_numpy(S.weights_f32(0, 300, 512)).to(device)
+    wq, sc, bi = q.quantize_affine(w, 4, sdtype=torch.float16)
+    x = S.activations(0, 1, 512, "f16").to(device)
+    y = torch.empty((1, 300), dtype=torch.float16, device=device)
+    t = time_flushed(lambda: q.qmv(x, wq, sc, bi, 4, out=y), device, flush)
+    b = wq.numel() * 4 + 2 * sc.numel() * 2 + (512 + 300) * 2
+    out["single_qmv_300x512_4bit"] = {"us": t * 1e6, "algorithmic_bytes": b,
+                                      "gbs": b / t / 1e9, "frac": b / t / 1e9 / peaks["hbm_gbs"]}
+    # one decoder layer, 4-bit, as the decode step runs it
+    layer = DecodeStep(device, bits=4, dtype=torch.float16, seed=1, layers=1, lm_head=False,
+                       prefetch_distance=min(prefetch_distance, 8 << 20))
+    layer.x0.copy_(S.activations(1, 1, 2048, "f16").to(device))
+    layer.capture()
+    t = time_flushed(layer.replay, device, flush)
+    b = sum(layer.algorithmic_bytes())
+    res = {"fused_4_launches_graph": {"us": t * 1e6, "algorithmic_bytes": b, "gbs": b / t / 1e9,
+                                      "frac": b / t / 1e9 / peaks["hbm_gbs"],
+                                      "prefetch_distance": layer.prefetch_distance}}
+    per = {}
+    for i, (name, n, k) in enumerate(S.LLAMA_1B_LINEARS):
+        _, _, _, _, lwq, lsc, lbi, wseed = layer.linear_rows(i)
+        lwq, lsc, lbi = lwq.contiguous(), lsc.contiguous(), lbi.contiguous()
+        xx = S.activations(wseed, 1, k, "f16").to(device)
+        yy = torch.empty((1, n), dtype=torch.float16, device=device)
+        t = time_flushed(lambda: q.qmv(xx, lwq, lsc, lbi, 4, out=yy), device, flush)
+        b = lwq.numel() * 4 + 2 * lsc.numel() * 2 + (k + n) * 2
+        per[name] = {"n": n, "k": k, "us": t * 1e6, "gbs": b / t / 1e9,
+                     "frac": b / t / 1e9 / peaks["hbm_gbs"]}
+    res["separate_launches"] = per
+    out["decoder_layer_4bit"] = res
+    del layer, flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def per_launch_durations(step, device, reps: int = 3):
-    """Each launch of the step bracketed by CUDA events on its stream.  A GPU
+    """Diagnostic: each launch of the step alone, bracketed by CUDA events on
+    its stream.  A GPU
     sleep is queued first so that the host enqueues every launch and event
     before the GPU reaches them: the events then time the kernels back to back
     (as in the graph), not the host's launch latency.  The launches here are
@@ -502,54 +673,33 @@ def qmm_chain_timing(q, device, m: int = 512, layers: int = 4, reps: int = 50):
     return res
 
 
-def dense_f16_step(q, step, device, steps: int):
+def dense_f16_step(step, device, steps: int):
     """The same decode step with every weight resident as dense f16 (built
     once with qlin_dequant, outside the timed region) and each linear run as
-    torch's F.linear (cuBLAS): the unfused f16 path the packed kernels replace.
+    torch.matmul (cuBLAS): the unfused f16 path the packed kernels replace.
     Same chaining, one CUDA graph, same number of replays."""
     import torch
-    import torch.nn.functional as F
 
-    ws = [q.dequant(u["wq"], u["scales"], u["biases"], step.bits) for u in step.units]
-    outs = [torch.empty_like(u["out"]) for u in step.units]
-
-    def input_of(i):
-        name = step.units[i]["name"]
-        if i == 0:
-            return step.x0
-        prev = outs[i - 1]
-        if name == "o":
-            return prev[:, :2048]
-        if name == "down":
-            return prev[:, :8192]
-        return prev
-
-    def run():
-        for i in range(len(ws)):
-            torch.matmul(input_of(i), ws[i].t(), out=outs[i])
-
-    run()
-    torch.cuda.synchronize(device)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        run()
+    from int8_qmv_qmm_gb300.decode_step import DenseF16Step
+    dense = DenseF16Step(step)
+    dense.capture()
     for _ in range(3):
-        g.replay()
+        dense.replay()
     torch.cuda.synchronize(device)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda._sleep(20_000_000)
     e0.record()
     for _ in range(steps):
-        g.replay()
+        dense.replay()
     e1.record()
     torch.cuda.synchronize(device)
     t = e0.elapsed_time(e1) * 1e-3 / steps
-    dense_bytes = sum(w.numel() * 2 for w in ws)
-    del ws, outs, g
+    dense_bytes = dense.weight_bytes()
+    del dense
     torch.cuda.empty_cache()
     return {"tokens_per_s": 1.0 / t, "ms_per_step": t * 1e3, "weight_bytes": dense_bytes,
-            "gbs": dense_bytes / t / 1e9, "how": "dense f16 weights, torch F.linear (cuBLAS), "
+            "gbs": dense_bytes / t / 1e9, "how": "dense f16 weights, torch.matmul (cuBLAS), "
             "one CUDA graph of the same 65 chained linears"}
 
 
@@ -569,7 +719,8 @@ def bench_ours(args):
     q.lib()
     peaks = load_peaks()
 
-    step = DecodeStep(device, bits=8, dtype=torch.float16, seed=2, mode="launches")
+    step = DecodeStep(device, bits=8, dtype=torch.float16, seed=2, mode="launches",
+                      prefetch_distance=args.prefetch_mb << 20)
     x_host = torch.randn((1, 2048), generator=torch.Generator().manual_seed(0)).to(
         torch.float16).pin_memory()
     step.x0.copy_(x_host)
@@ -592,11 +743,13 @@ def bench_ours(args):
     per_step = t / args.steps
     value = replica_throughput(world, args.steps, t)
 
-    # ---- the dominant kernel (qmv) launch by launch, CUDA events on its stream
+    # ---- the dominant kernel (qmv): its launches are the whole graph, so its
+    # average launch duration over the timed region is per_step / launches
     alg_list = step.algorithmic_bytes()
     alg = sum(alg_list)
+    achieved = alg / per_step / 1e9
+    # diagnostic: each launch alone (no overlap), CUDA events around it
     durs = per_launch_durations(step, device)
-    achieved = alg / sum(durs) / 1e9
     top = max(range(step.n_launches), key=lambda i: durs[i])
 
     # ---- the same step as one persistent chain launch (qlin_qmv_chain), for comparison
@@ -610,7 +763,7 @@ def bench_ours(args):
     step.capture()
 
     # ---- the unfused comparator: the same step on dense f16 weights (cuBLAS)
-    dense = dense_f16_step(q, step, device, args.steps)
+    dense = dense_f16_step(step, device, args.steps)
 
     # ---- end to end through the public API with host buffers
     logits_host = torch.empty((1, step.logits.shape[1]), dtype=torch.float16).pin_memory()
@@ -625,6 +778,7 @@ def bench_ours(args):
     t_e2e = max_over_ranks(dist, time.perf_counter() - t0, device)
     e2e_value = world * args.steps / t_e2e
 
+    small = small_workloads(q, device, peaks, step.prefetch_distance)
     qmm_res = None if args.no_qmm else time_qmm(q, device, peaks)
     qmm_chain = None if args.no_qmm else qmm_chain_timing(q, device)
     cross = None if args.no_qmm else crossover_sweep(q, device)
@@ -651,18 +805,27 @@ def bench_ours(args):
         "qmv_step_frac_of_peak": bytes_step / per_step / 1e9 / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                     "kernel": "qmv_kernel (the %d launches of a step, each timed with events)"
-                               % step.n_launches,
+                     "kernel": "qmv_kernel: the %d launches of a step, which make up the whole "
+                               "timed graph; average launch = ms_per_step / %d"
+                               % (step.n_launches, step.n_launches),
                      "algorithmic_bytes_per_launch": alg / step.n_launches,
-                     "mean_launch_us": sum(durs) / len(durs) * 1e6,
+                     "mean_launch_us": per_step / step.n_launches * 1e6,
                      "peak_source": peaks["source"],
-                     "per_shape": per_shape_summary(step, durs, alg_list),
-                     "largest_launch": {"name": step.units[top]["name"], "us": durs[top] * 1e6,
-                                        "gbs": alg_list[top] / durs[top] / 1e9}},
+                     "prefetch_distance_bytes": step.prefetch_distance},
+        "isolated_launches": {"note": "diagnostic: each launch of the step alone, no overlap "
+                                      "with its neighbours, CUDA events around it",
+                              "sum_us": sum(durs) * 1e6,
+                              "per_shape": per_shape_summary(step, durs, alg_list),
+                              "largest_launch": {"name": step.units[top]["name"],
+                                                 "us": durs[top] * 1e6,
+                                                 "gbs": alg_list[top] / durs[top] / 1e9}},
+        "small_workloads": small,
         "chain_mode": {"tokens_per_s": world * args.steps / t_c,
                        "kernel_us": chain_s * 1e6,
                        "kernel_gbs": alg / chain_s / 1e9},
-        "dense_f16_step": dict(dense, packed_speedup=value / world / dense["tokens_per_s"]),
+        "dense_f16_step": dense,
+        "dense_f16_tokens_per_s": dense["tokens_per_s"],
+        "packed_speedup_vs_dense_f16": value / world / dense["tokens_per_s"],
         "qmm": qmm_res,
         "qmm_chain": qmm_chain,
         "crossover": cross,
@@ -677,21 +840,24 @@ def bench_ours(args):
 
 
 def bench_reference(args):
-    """The reference arm: the CPU oracle as it stands, each step a bounded
-    sample (every REFERENCE_STRIDE-th output row) of the same decode step."""
+    """The reference arm: the CPU oracle as it stands, on every host core,
+    each step one whole decode step of the same workload (all 113 linears,
+    every output row)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and rank != 0:
         return
-    r = run_oracle(REFERENCE_STRIDE, args.steps)
+    cores = host_cores()
+    r = run_oracle(cores, 1, max(1, args.warmup), args.steps, budget_s=150)
     value = r["value"]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["s_per_pass"] * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD},
-        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": r["sample"],
+        "cpu_baseline": {"kind": "oracle", "cores": cores, "sample": r["sample"],
                          "value": value, "unit": UNIT},
+        "sample_fraction": r["fraction"], "value_extrapolated": r["extrapolated"],
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -732,7 +898,7 @@ def profile_case(which: str, launches: int = 3):
 
 def main():
     if len(sys.argv) >= 2 and sys.argv[1] == "--oracle-child":
-        print(json.dumps(oracle_sample_child(int(sys.argv[2]), int(sys.argv[3]))), flush=True)
+        print(json.dumps(oracle_steps_child(*(int(v) for v in sys.argv[2:7]))), flush=True)
         return
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -741,6 +907,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-qmm", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefetch-mb", type=int, default=DEFAULT_PREFETCH_MB,
+                    help="L2 prefetch distance of the decode step's launches (0: none)")
     ap.add_argument("--profile", choices=["qmv", "qmv_o", "qmv_gate_up", "qmv_down", "qmm",
                                           "qmm8", "qmm_sq", "qmm_split"],
                     help="run a small fixed case for ncu instead of the benchmark")

@@ -38,7 +38,9 @@
  *
  * Errors: every call validates its arguments on the host before anything is
  * launched and returns a status; on failure nothing was launched and
- * qlin_last_error() (per calling thread) describes why.  A launch failure
+ * qlin_last_error() (per calling thread) describes why.  The pages' own guards
+ * likewise make unsupported settings fail fast instead of faulting mid-run
+ * ("track(upstream-iree): ...", section "What is already in-tree").  A launch failure
  * reported by the CUDA runtime returns QLIN_ERR_CUDA.  Calls are asynchronous
  * on the given stream (a cudaStream_t passed as void*; NULL = legacy default
  * stream) and never synchronise the device.
@@ -67,14 +69,18 @@ typedef enum {
 
 typedef enum { QLIN_F32 = 0, QLIN_F16 = 1, QLIN_BF16 = 2 } qlin_dtype;
 
-/* Human-readable name of a status code (static string). */
+/* Human-readable name of a status code (static string).  No counterpart on
+ * the pages: an addition of this library. */
 const char* qlin_status_str(qlin_status s);
 
 /* Detail of the last failing call made by this thread (static per-thread
- * buffer; empty string if none). */
+ * buffer; empty string if none).  No counterpart on the pages: an addition of
+ * this library, in the spirit of the guards that fail fast with a reason
+ * ("track(upstream-iree): ...", section "What is already in-tree"). */
 const char* qlin_last_error(void);
 
-/* Library version as 10000*major + 100*minor + patch. */
+/* Library version as 10000*major + 100*minor + patch.  No counterpart on the
+ * pages: an addition of this library. */
 int qlin_version(void);
 
 /*
@@ -116,13 +122,25 @@ qlin_status qlin_dequant(const uint32_t* wq, const void* scales, const void* bia
  * scales and biases.  Correct for any M >= 1 and N >= 1 (N need not be a
  * multiple of 4); fastest for M <= 4.  Alignment: x and wq 16-byte aligned.
  * Streams each packed word, scale and bias once per M-tile of 4 rows of x.
+ * Defining passages: the reconstruction is consumed inside the product and
+ * never written to DRAM ("track(upstream-iree): ...", section "The blocker
+ * (measured)"); the M = 1 product for any N, including N not a multiple of 4
+ * ("Metal backend: import qmv_impl from MLX").
+ *
+ * No workspace argument: the kernel gives each CTA whole rows and reduces
+ * within a warp, so it needs no scratch memory, and the workspace pointer and
+ * size query that a split-K design would need are not part of the call.
  */
 qlin_status qlin_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
                      qlin_dtype dtype, void* stream);
 
 /*
- * Launch flags for the *_ex entry points.
+ * Launch flags for the *_ex entry points.  No counterpart on the pages: an
+ * addition of this library, aimed at the launch gaps between dependent
+ * linears (the pages count ~678 dispatches per packed decode step: "epic:
+ * realize low-precision / quantized performance on the OpenXLA (IREE)
+ * backend", section "The measured fusion gate").
  *
  * QLIN_OVERLAP_PREVIOUS: launch as a programmatic dependent launch.  The
  *   kernel may start while the preceding kernel on the stream is still
@@ -135,10 +153,45 @@ qlin_status qlin_qmv(const void* x, const uint32_t* wq, const void* scales, cons
 #define QLIN_OVERLAP_PREVIOUS 1u
 
 /* qlin_qmv with launch flags (0 = same as qlin_qmv).  Unknown flag bits
- * return QLIN_ERR_INVALID_ARG. */
+ * return QLIN_ERR_INVALID_ARG.  Product as qlin_qmv (same passages); the
+ * flags are an addition of this library. */
 qlin_status qlin_qmv_ex(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                         void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
                         qlin_dtype dtype, unsigned flags, void* stream);
+
+/*
+ * Prefetch ahead of a weight stream.  No counterpart on the pages: an
+ * addition of this library, aimed at the cost the pages trace to a decode
+ * step of many dependent dispatches ("epic: realize low-precision / quantized
+ * performance on the OpenXLA (IREE) backend", section "The measured fusion
+ * gate").
+ *
+ * A decode step reads the weights of its linears once each, in a fixed
+ * order, and each linear waits for the previous one's output.  When all the
+ * weights of the step lie in one device region in launch order, a launch can
+ * ask L2 to fetch the region's bytes `distance` ahead of what it reads
+ * itself, so that HBM keeps streaming while dependent launches wait for each
+ * other, and later launches find their weights in L2.  The prefetch is a hint:
+ * results do not depend on it.
+ */
+typedef struct {
+  const void* base;   /* start of the region (device memory, 16-byte aligned) */
+  uint64_t bytes;     /* size of the region, a multiple of 16; prefetching wraps
+                         around at its end (a decode loop reads it again) */
+  uint64_t offset;    /* where this launch's weights (wq, scales, biases) start */
+  uint64_t span;      /* bytes of this launch's weights in the region, padding
+                         included; wq must lie in [offset, offset + span) */
+  uint64_t distance;  /* prefetch distance in region bytes; 0: no prefetch */
+} qlin_prefetch;
+
+/* qlin_qmv_ex with a prefetch ahead of the weight stream (pf may be NULL:
+ * same as qlin_qmv_ex).  Errors as qlin_qmv_ex; a region that is misaligned,
+ * not a multiple of 16 bytes, or does not hold wq where pf says returns
+ * QLIN_ERR_INVALID_ARG / QLIN_ERR_MISALIGNED. */
+qlin_status qlin_qmv_prefetch(const void* x, const uint32_t* wq, const void* scales,
+                              const void* biases, void* y, int64_t M, int64_t N, int64_t K,
+                              int bits, int group_size, qlin_dtype dtype, unsigned flags,
+                              const qlin_prefetch* pf, void* stream);
 
 /*
  * A chain of dependent M = 1 products in one launch (a decode step).
@@ -166,7 +219,8 @@ typedef struct {
 } qlin_link;
 
 /* Bytes of device scratch qlin_qmv_chain needs for n_links links (one 32-bit
- * completion counter per link, rounded up to 256 bytes). */
+ * completion counter per link, rounded up to 256 bytes).  No counterpart on
+ * the pages: an addition of this library. */
 size_t qlin_qmv_chain_workspace_size(int n_links);
 
 /*
@@ -209,8 +263,14 @@ qlin_status qlin_qmv_chain_static(const void* x0, const qlin_link* links, int n_
  * A operand of tcgen05 MMAs with f32 accumulators in tensor memory; when the
  * output has few tiles, K is split over a thread-block cluster and the
  * partial sums are added through distributed shared memory (no workspace).
- * Same arguments and result contract as qlin_qmv.  Extra requirement:
- * K % 64 == 0 (always true for group 64) and x, wq 16-byte aligned.
+ * Same arguments and result contract as qlin_qmv: for dtype QLIN_BF16 the
+ * tensor-core operand carries w_hat as bf16 hi plus a bf16 residual lo (two
+ * MMAs per K step), so rounding the operand to bf16 costs no accuracy.  Extra
+ * requirement: K % 64 == 0 (always true for group 64) and x, wq 16-byte
+ * aligned.  Defining passages: the target must fuse the dequantisation into
+ * the matmul ("track(upstream-iree): ...", sections "The blocker (measured)"
+ * and "Unblock criteria"), with bf16 scales and biases accepted (same page,
+ * "What is already in-tree").
  */
 qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
@@ -220,19 +280,25 @@ qlin_status qlin_qmm(const void* x, const uint32_t* wq, const void* scales, cons
  * as for qlin_qmv_ex: the launch and the kernel's set-up (barriers, tensor
  * memory, descriptor prefetch) overlap the preceding kernel on the stream; x
  * is read and y written only after that kernel has completed.  Unknown flag
- * bits return QLIN_ERR_INVALID_ARG. */
+ * bits return QLIN_ERR_INVALID_ARG.  Product as qlin_qmm (same passages); the
+ * flags are an addition of this library. */
 qlin_status qlin_qmm_ex(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                         void* y, int64_t M, int64_t N, int64_t K, int bits, int group_size,
                         qlin_dtype dtype, unsigned flags, void* stream);
 
 /*
  * Dispatch to qlin_qmv when M < qlin_crossover_m(N, K, bits), else qlin_qmm.
+ * The product is the one both kernels define (same passages); choosing
+ * between them by M is an addition of this library.
  */
 qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
                         const void* biases, void* y, int64_t M, int64_t N, int64_t K, int bits,
                         int group_size, qlin_dtype dtype, void* stream);
 
-/* Smallest M for which qlin_linear picks the tensor-core path (measured). */
+/* Smallest M for which qlin_linear picks the tensor-core path, from
+ * measurements on GB300; the environment variable QLIN_CROSSOVER_M (read once
+ * per process) overrides it.  No counterpart on the pages: an addition of
+ * this library. */
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits);
 
 /*
@@ -245,9 +311,10 @@ int64_t qlin_crossover_m(int64_t N, int64_t K, int bits);
  *   own bias vector, not the quantisation biases of the packed format.)
  * y_dtype: QLIN_F32 (y is float [M][N], 4-byte aligned, no rounding) or the
  *   activation dtype (y as in qlin_linear).
- * The pages' ExecuTorch stack ships a 4-bit linear with bias ("feat: extend
- * the fused low-precision path to the Metal target", results table); the
- * f32 output serves callers that keep the residual stream in f32.
+ * The pages' ExecuTorch stack ships a 4-bit linear with bias ("Metal backend:
+ * import qmv_impl from MLX", its stack of changes: "enable linear with bias",
+ * "test 4-bit linear with bias"); the f32 output serves callers that keep the
+ * residual stream in f32 (an addition of this library).
  *
  * Errors: as qlin_linear; y_dtype other than QLIN_F32 or dtype is
  * QLIN_ERR_UNSUPPORTED; layer_bias not 2-byte or an f32 y not 4-byte aligned
@@ -264,7 +331,9 @@ qlin_status qlin_linear_ex(const void* x, const uint32_t* wq, const void* scales
  * the last call, else a bit mask of the waits that gave up (bits 0-7: the
  * tensor-core kernel, bits 8-15: the CUDA-core kernel, bits 16-23: the chain
  * kernel).  Returns QLIN_OK, or
- * QLIN_ERR_CUDA if the device could not be read.
+ * QLIN_ERR_CUDA if the device could not be read.  No counterpart on the pages:
+ * an addition of this library (a kernel that gives up a wait reports instead
+ * of hanging, the device-side form of failing fast).
  */
 qlin_status qlin_device_status(int* flags);
 

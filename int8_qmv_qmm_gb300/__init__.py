@@ -25,7 +25,7 @@ from .build_lib import LIB_PATH
 __all__ = [
     "QlinError", "lib", "quantize_affine", "dequant", "qmv", "qmm", "linear",
     "crossover_m", "device_status", "QLIN_F32", "QLIN_F16", "QLIN_BF16", "Link", "make_links",
-    "chain_workspace", "qmv_chain",
+    "chain_workspace", "qmv_chain", "Prefetch",
 ]
 
 QLIN_F32, QLIN_F16, QLIN_BF16 = 0, 1, 2
@@ -46,6 +46,8 @@ _SIGNATURES = {
                               _c_vp, _c_vp]),
     "qlin_qmv": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_qmv_ex": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [ctypes.c_uint, _c_vp]),
+    "qlin_qmv_prefetch": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 +
+                          [ctypes.c_uint, _c_vp, _c_vp]),
     "qlin_qmm": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_qmm_ex": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [ctypes.c_uint, _c_vp]),
     "qlin_linear": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
@@ -70,6 +72,12 @@ class Link(ctypes.Structure):
     _fields_ = [("wq", _c_vp), ("scales", _c_vp), ("biases", _c_vp), ("y", _c_vp),
                 ("N", _c_i64), ("K", _c_i64), ("input", ctypes.c_int32),
                 ("input_offset", ctypes.c_int32)]
+
+
+class Prefetch(ctypes.Structure):
+    """qlin_prefetch: L2 prefetch ahead of a weight stream (include/qlin.h)."""
+    _fields_ = [("base", _c_vp), ("bytes", ctypes.c_uint64), ("offset", ctypes.c_uint64),
+                ("span", ctypes.c_uint64), ("distance", ctypes.c_uint64)]
 
 
 class QlinError(RuntimeError):
@@ -119,15 +127,26 @@ def _need_cuda(*ts):
 
 
 def quantize_affine(w: torch.Tensor, bits: int, group_size: int = GROUP_SIZE,
-                    sdtype: torch.dtype = torch.float16):
-    """Quantise float32 W[N, K] on the GPU -> (wq, scales, biases)."""
+                    sdtype: torch.dtype = torch.float16, out=None):
+    """Quantise float32 W[N, K] on the GPU -> (wq, scales, biases).
+
+    out: optional (wq, scales, biases) tensors to write into (e.g. views of
+    one weight region)."""
     _need_cuda(w)
     if w.dtype != torch.float32 or w.dim() != 2:
         raise ValueError("w must be a 2-D float32 tensor")
     n, k = w.shape
-    wq = torch.empty((n, k * bits // 32), dtype=torch.int32, device=w.device)
-    sc = torch.empty((n, k // group_size), dtype=sdtype, device=w.device)
-    bi = torch.empty_like(sc)
+    if out is not None:
+        wq, sc, bi = out
+        _need_cuda(wq, sc, bi)
+        if (tuple(wq.shape) != (n, k * bits // 32) or tuple(sc.shape) != (n, k // group_size)
+                or tuple(bi.shape) != tuple(sc.shape) or sc.dtype != sdtype
+                or bi.dtype != sdtype or wq.element_size() != 4):
+            raise ValueError("out tensors do not match W's shape, bits and scale dtype")
+    else:
+        wq = torch.empty((n, k * bits // 32), dtype=torch.int32, device=w.device)
+        sc = torch.empty((n, k // group_size), dtype=sdtype, device=w.device)
+        bi = torch.empty_like(sc)
     _check(lib().qlin_quantize_affine(_ptr(w), n, k, bits, group_size, _DTYPE_CODE[sdtype],
                                       _ptr(wq), _ptr(sc), _ptr(bi), _stream(w)))
     return wq, sc, bi
@@ -147,7 +166,7 @@ def dequant(wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor, bits: 
     return out
 
 
-def _matmul(name: str, x, wq, scales, biases, bits, group_size, out, flags=None):
+def _matmul(name: str, x, wq, scales, biases, bits, group_size, out, flags=None, extra=()):
     _need_cuda(x, wq, scales, biases)
     if x.dim() != 2:
         raise ValueError("x must be 2-D [M, K]")
@@ -159,18 +178,25 @@ def _matmul(name: str, x, wq, scales, biases, bits, group_size, out, flags=None)
         out = torch.empty((m, n), dtype=x.dtype, device=x.device)
     _need_cuda(out)
     fn = getattr(lib(), name)
-    extra = () if flags is None else (flags,)
+    args = (() if flags is None else (flags,)) + tuple(extra)
     _check(fn(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(out), m, n, k, bits,
-              group_size, _DTYPE_CODE[x.dtype], *extra, _stream(x)))
+              group_size, _DTYPE_CODE[x.dtype], *args, _stream(x)))
     return out
 
 
-def qmv(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None, overlap_previous=False):
+def qmv(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None, overlap_previous=False,
+        prefetch=None):
     """y = x . w_hat^T on CUDA cores (decode, small M).
 
     overlap_previous=True launches with QLIN_OVERLAP_PREVIOUS (programmatic
     dependent launch): only valid when the preceding work on the stream does
-    not write wq/scales/biases."""
+    not write wq/scales/biases.  prefetch: a Prefetch (qlin_qmv_prefetch) that
+    places this launch's weights in a stream region and asks L2 to fetch the
+    region ahead of them."""
+    if prefetch is not None:
+        return _matmul("qlin_qmv_prefetch", x, wq, scales, biases, bits, group_size, out,
+                       flags=QLIN_OVERLAP_PREVIOUS if overlap_previous else 0,
+                       extra=(ctypes.byref(prefetch),))
     if overlap_previous:
         return _matmul("qlin_qmv_ex", x, wq, scales, biases, bits, group_size, out,
                        flags=QLIN_OVERLAP_PREVIOUS)

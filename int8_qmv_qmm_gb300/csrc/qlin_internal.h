@@ -33,10 +33,12 @@ struct Epilogue {
 
 qlin_status launch_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, const Epilogue& ep, cudaStream_t st);
+                       unsigned flags, const Epilogue& ep, cudaStream_t st,
+                       const qlin_prefetch* pf = nullptr);
 qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, const Epilogue& ep, cudaStream_t st);
+                       unsigned flags, const Epilogue& ep, cudaStream_t st,
+                       const qlin_prefetch* pf = nullptr);  // pf: ignored
 
 // Limits of the chain kernel's waits for an input link.  stalled_link >= 0
 // (tests only) makes the readers of that link wait for one row block more

@@ -27,30 +27,41 @@ from __future__ import annotations
 
 import torch
 
-from . import chain_workspace, make_links, qmv, qmv_chain, quantize_affine
+from . import Prefetch, chain_workspace, dequant, make_links, qmv, qmv_chain, quantize_affine
 from . import synthetic as S
 
 _FUSED = (("qkv", ("q_proj", "k_proj", "v_proj")), ("o", ("o_proj",)),
           ("gate_up", ("gate_proj", "up_proj")), ("down", ("down_proj",)))
 
 
+def _round_up(v: int, a: int = 256) -> int:
+    return (v + a - 1) // a * a
+
+
 class DecodeStep:
     def __init__(self, device, bits: int = 8, dtype: torch.dtype = torch.float16,
                  seed: int = 2, layers: int = S.LLAMA_1B_LAYERS, lm_head: bool = True,
-                 overlap: bool = True, mode: str = "launches"):
+                 overlap: bool = True, mode: str = "launches", prefetch_distance: int = 0):
         """mode "launches": one qlin_qmv launch per fused linear (overlapped
         with programmatic dependent launch when ``overlap``; the faster mode on
-        GB300); mode "chain": the whole step is one qlin_qmv_chain launch."""
+        GB300); mode "chain": the whole step is one qlin_qmv_chain launch.
+
+        All packed weights, scales and biases live in one device region, in
+        launch order (each piece 256-byte aligned).  prefetch_distance > 0
+        makes every launch ask L2 for the region's bytes that far ahead of
+        what it reads itself (qlin_qmv_prefetch), so that HBM keeps streaming
+        while the dependent launches wait for each other."""
         self.device = torch.device(device)
         self.bits = bits
         self.dtype = dtype
         self.overlap = overlap
         self.mode = mode
+        self.prefetch_distance = int(prefetch_distance)
         shapes = {name: (n, k) for name, n, k in S.LLAMA_1B_LINEARS}
         # original linears, in the order of the weight seeds:
         # (name, layer, N, K, unit index, first row in the unit, weight seed)
         self.linears = []
-        self.units = []  # dicts: name, layer, N, K, wq, scales, biases, out
+        specs = []  # per unit: name, layer, N, K, [(weight seed, rows)]
         idx = 0
         for layer in range(layers):
             seeds = {}
@@ -59,23 +70,56 @@ class DecodeStep:
                 idx += 1
             for uname, parts in _FUSED:
                 k = shapes[parts[0]][1]
-                rows, ws = 0, []
+                rows, srcs = 0, []
                 for p in parts:
                     n = shapes[p][0]
-                    self.linears.append((p, layer, n, k, len(self.units), rows, seeds[p]))
-                    ws.append(torch.from_numpy(S.weights_f32(seeds[p], n, k)))
+                    self.linears.append((p, layer, n, k, len(specs), rows, seeds[p]))
+                    srcs.append((seeds[p], n))
                     rows += n
-                self._add_unit(uname, layer, torch.cat(ws).to(self.device))
+                specs.append((uname, layer, rows, k, srcs))
         if lm_head:
             name, n, k = S.LLAMA_1B_LM_HEAD
             wseed = S.weight_seed(seed, idx)
-            self.linears.append((name, layers, n, k, len(self.units), 0, wseed))
-            self._add_unit(name, layers, torch.from_numpy(S.weights_f32(wseed, n, k)).to(self.device))
+            self.linears.append((name, layers, n, k, len(specs), 0, wseed))
+            specs.append((name, layers, n, k, [(wseed, n)]))
+        # the weight region: wq, scales, biases of every unit in launch order
+        es = torch.empty((), dtype=dtype).element_size()
+        offs, total = [], 0
+        for (_, _, n, k, _) in specs:
+            wq_b, sc_b = n * k * bits // 8, n * (k // 64) * es
+            offs.append((total, total + _round_up(wq_b), total + _round_up(wq_b) + _round_up(sc_b)))
+            total += _round_up(wq_b) + 2 * _round_up(sc_b)
+        self.region = torch.empty(total, dtype=torch.uint8, device=self.device)
+        self.units = []  # dicts: name, layer, N, K, wq, scales, biases, out, offset, span
+        for (uname, layer, n, k, srcs), (o_w, o_s, o_b) in zip(specs, offs):
+            wq_b, sc_b = n * k * bits // 8, n * (k // 64) * es
+            views = (self.region[o_w:o_w + wq_b].view(torch.int32).view(n, k * bits // 32),
+                     self.region[o_s:o_s + sc_b].view(dtype).view(n, k // 64),
+                     self.region[o_b:o_b + sc_b].view(dtype).view(n, k // 64))
+            w = torch.cat([torch.from_numpy(S.weights_f32(ws, wn, k)) for ws, wn in srcs])
+            quantize_affine(w.to(self.device), bits, sdtype=dtype, out=views)
+            del w
+            end = o_b + _round_up(sc_b)
+            self.units.append(dict(name=uname, layer=layer, N=n, K=k, wq=views[0],
+                                   scales=views[1], biases=views[2],
+                                   out=torch.empty((1, n), dtype=dtype, device=self.device),
+                                   offset=o_w, span=end - o_w))
         self.layers = layers
         hidden = S.LLAMA_1B_LINEARS[0][2]
         self.x0 = torch.zeros((1, hidden), dtype=dtype, device=self.device)
         self.graph = None
+        self._set_prefetch()
         self._build_chain()
+
+    def _set_prefetch(self):
+        self._prefetch = [None if self.prefetch_distance <= 0 else
+                          Prefetch(self.region.data_ptr(), self.region.numel(), u["offset"],
+                                   u["span"], self.prefetch_distance) for u in self.units]
+
+    def set_prefetch_distance(self, distance: int):
+        """Change the prefetch distance (recapture the graph afterwards)."""
+        self.prefetch_distance = int(distance)
+        self._set_prefetch()
 
     def _build_chain(self):
         """The link table of the step (same chaining as input_of)."""
@@ -96,14 +140,6 @@ class DecodeStep:
                               K=d["K"], input=inp, input_offset=off))
         self._links = make_links(links)
         self._workspace = chain_workspace(len(links), self.device)
-
-    def _add_unit(self, name, layer, w):
-        n, k = w.shape
-        wq, sc, bi = quantize_affine(w, self.bits, sdtype=self.dtype)
-        del w
-        out = torch.empty((1, n), dtype=self.dtype, device=self.device)
-        self.units.append(dict(name=name, layer=layer, N=n, K=k, wq=wq, scales=sc, biases=bi,
-                               out=out))
 
     # ------------------------------------------------------------------ sizes
     @property
@@ -139,7 +175,8 @@ class DecodeStep:
                overlap: bool = False):
         d = self.units[u]
         return qmv(x, d["wq"], d["scales"], d["biases"], self.bits,
-                   out=d["out"] if out is None else out, overlap_previous=overlap)
+                   out=d["out"] if out is None else out, overlap_previous=overlap,
+                   prefetch=self._prefetch[u])
 
     def launch_chain(self):
         qmv_chain(self.x0, self._links, len(self.units), self.bits, self.dtype, self._workspace)
@@ -190,3 +227,56 @@ class DecodeStep:
         out = torch.empty((x.shape[0], self.units[u]["N"]), dtype=self.dtype, device=self.device)
         self.launch(u, x, out=out)
         return out[:, r0:r0 + n]
+
+
+class DenseF16Step:
+    """The same decode step with every weight resident as a dense matrix in
+    the activation dtype, materialised once by qlin_dequant, and each linear
+    run by torch.matmul (cuBLAS): the unfused, f16-resident path that the
+    packed one has to beat ("epic: realize low-precision / quantized
+    performance on the OpenXLA (IREE) backend", section "Thesis", item 1;
+    "track(upstream-iree): fused dequant->matmul for the packed int8 bandwidth
+    win", section "Unblock criteria").  A comparator, not the product path."""
+
+    def __init__(self, step: DecodeStep):
+        self.step = step
+        self.weights = [dequant(u["wq"], u["scales"], u["biases"], step.bits)
+                        for u in step.units]
+        self.outs = [torch.empty_like(u["out"]) for u in step.units]
+        self.graph = None
+
+    def weight_bytes(self) -> int:
+        return sum(w.numel() * w.element_size() for w in self.weights)
+
+    def input_of(self, u: int) -> torch.Tensor:
+        """Same chaining as DecodeStep.input_of, on this step's outputs."""
+        name = self.step.units[u]["name"]
+        if u == 0:
+            return self.step.x0
+        prev = self.outs[u - 1]
+        if name == "o":
+            return prev[:, :2048]
+        if name == "down":
+            return prev[:, :8192]
+        return prev
+
+    def run_step(self):
+        for u, w in enumerate(self.weights):
+            torch.matmul(self.input_of(u), w.t(), out=self.outs[u])
+
+    def capture(self):
+        self.run_step()
+        torch.cuda.synchronize(self.step.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run_step()
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+
+    def run_linear(self, i: int, x: torch.Tensor) -> torch.Tensor:
+        """Original linear ``i`` on an arbitrary input."""
+        name, layer, n, k, u, r0, wseed = self.step.linears[i]
+        return torch.matmul(x, self.weights[u][r0:r0 + n].t())

@@ -251,8 +251,8 @@ def matmul_bias_ref(x, w_hat, layer_bias):
     term of each output's sum).
 
     layer_bias[N] is a linear layer's own bias vector (the ExecuTorch stack's
-    "4-bit linear with bias": "feat: extend the fused low-precision path to
-    the Metal target", results table), not the quantisation biases.
+    "4-bit linear with bias": "Metal backend: import qmv_impl from MLX", its
+    stack of changes), not the quantisation biases.
     """
     y_ref, a_ref = matmul_ref(x, w_hat)
     b64 = np.asarray(layer_bias, dtype=np.float64)

@@ -101,3 +101,29 @@ def test_full_decode_step_sampled_rows(dev):
     torch.cuda.synchronize()
     assert torch.equal(first, step.logits)
     assert q.device_status() == 0
+
+
+def test_dense_f16_comparator_computes_the_same_step(dev):
+    """The f16-resident comparator (dense weights from qlin_dequant, cuBLAS)
+    and the packed kernels compute the same linears: sampled rows of every
+    linear of a two-layer step with the lm_head, each on fresh input, agree
+    with the oracle within the tolerance on both paths; the dense step's
+    graph replays to finite logits."""
+    from int8_qmv_qmm_gb300.decode_step import DecodeStep, DenseF16Step
+    step = DecodeStep(dev, bits=8, dtype=torch.float16, seed=2, layers=2)
+    dense = DenseF16Step(step)
+    rng = np.random.default_rng(1)
+    for i in range(len(step.linears)):
+        name, layer, n, k, wq, sc, bi, wseed = step.linear_rows(i)
+        rows = np.unique(np.concatenate([[0, n - 1], rng.choice(n, 30, replace=False)]))
+        w_rows = S.weights_f32(wseed, n, k, rows=rows)
+        x = S.activations(wseed + 17, 1, k, "f16")
+        r = O.linear_ref(x.float().numpy().astype(np.float64), w_rows, 8, 64, "f16")
+        idx = torch.from_numpy(rows).to(dev)
+        assert_within_tolerance(step.run_linear(i, x.to(dev))[:, idx], r, f"packed {name}")
+        assert_within_tolerance(dense.run_linear(i, x.to(dev))[:, idx], r, f"dense {name}")
+    step.x0.copy_(S.activations(9, 1, 2048, "f16").to(dev))
+    dense.capture()
+    dense.replay()
+    torch.cuda.synchronize()
+    assert torch.isfinite(dense.outs[-1].float()).all()
