@@ -51,7 +51,6 @@ WORKLOAD = ("llama-3.2-1b-shaped decode step: 16 x (q 2048x2048, k 512x2048, v 5
             "earlier launch's output; launches overlapped with programmatic dependent launch; "
             "one CUDA graph")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DEFAULT_PREFETCH_MB = 0   # L2 prefetch distance of the decode step (measured best)
 
 
 # ------------------------------------------------------------------- helpers
@@ -498,7 +497,7 @@ def time_flushed(fn, device, flush, reps: int = 100, warm: int = 10):
     return statistics.median(ts)
 
 
-def small_workloads(q, device, peaks, prefetch_distance):
+def small_workloads(q, device, peaks):
     """The two M = 1 workloads below the L2 size, L2 flushed between timed
     repetitions: the single 300 x 512 qmv (4-bit) and one Llama-3.2-1B
     decoder layer's seven linears (4-bit), the latter both as the decode
@@ -520,15 +519,13 @@ def small_workloads(q, device, peaks, prefetch_distance):
     out["single_qmv_300x512_4bit"] = {"us": t * 1e6, "algorithmic_bytes": b,
                                       "gbs": b / t / 1e9, "frac": b / t / 1e9 / peaks["hbm_gbs"]}
     # one decoder layer, 4-bit, as the decode step runs it
-    layer = DecodeStep(device, bits=4, dtype=torch.float16, seed=1, layers=1, lm_head=False,
-                       prefetch_distance=min(prefetch_distance, 8 << 20))
+    layer = DecodeStep(device, bits=4, dtype=torch.float16, seed=1, layers=1, lm_head=False)
     layer.x0.copy_(S.activations(1, 1, 2048, "f16").to(device))
     layer.capture()
     t = time_flushed(layer.replay, device, flush)
     b = sum(layer.algorithmic_bytes())
     res = {"fused_4_launches_graph": {"us": t * 1e6, "algorithmic_bytes": b, "gbs": b / t / 1e9,
-                                      "frac": b / t / 1e9 / peaks["hbm_gbs"],
-                                      "prefetch_distance": layer.prefetch_distance}}
+                                      "frac": b / t / 1e9 / peaks["hbm_gbs"]}}
     per = {}
     for i, (name, n, k) in enumerate(S.LLAMA_1B_LINEARS):
         _, _, _, _, lwq, lsc, lbi, wseed = layer.linear_rows(i)
@@ -719,8 +716,7 @@ def bench_ours(args):
     q.lib()
     peaks = load_peaks()
 
-    step = DecodeStep(device, bits=8, dtype=torch.float16, seed=2, mode="launches",
-                      prefetch_distance=args.prefetch_mb << 20)
+    step = DecodeStep(device, bits=8, dtype=torch.float16, seed=2, mode="launches")
     x_host = torch.randn((1, 2048), generator=torch.Generator().manual_seed(0)).to(
         torch.float16).pin_memory()
     step.x0.copy_(x_host)
@@ -778,7 +774,7 @@ def bench_ours(args):
     t_e2e = max_over_ranks(dist, time.perf_counter() - t0, device)
     e2e_value = world * args.steps / t_e2e
 
-    small = small_workloads(q, device, peaks, step.prefetch_distance)
+    small = small_workloads(q, device, peaks)
     qmm_res = None if args.no_qmm else time_qmm(q, device, peaks)
     qmm_chain = None if args.no_qmm else qmm_chain_timing(q, device)
     cross = None if args.no_qmm else crossover_sweep(q, device)
@@ -810,8 +806,7 @@ def bench_ours(args):
                                % (step.n_launches, step.n_launches),
                      "algorithmic_bytes_per_launch": alg / step.n_launches,
                      "mean_launch_us": per_step / step.n_launches * 1e6,
-                     "peak_source": peaks["source"],
-                     "prefetch_distance_bytes": step.prefetch_distance},
+                     "peak_source": peaks["source"]},
         "isolated_launches": {"note": "diagnostic: each launch of the step alone, no overlap "
                                       "with its neighbours, CUDA events around it",
                               "sum_us": sum(durs) * 1e6,
@@ -907,8 +902,6 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-qmm", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--prefetch-mb", type=int, default=DEFAULT_PREFETCH_MB,
-                    help="L2 prefetch distance of the decode step's launches (0: none)")
     ap.add_argument("--profile", choices=["qmv", "qmv_o", "qmv_gate_up", "qmv_down", "qmm",
                                           "qmm8", "qmm_sq", "qmm_split"],
                     help="run a small fixed case for ncu instead of the benchmark")

@@ -160,40 +160,6 @@ qlin_status qlin_qmv_ex(const void* x, const uint32_t* wq, const void* scales, c
                         qlin_dtype dtype, unsigned flags, void* stream);
 
 /*
- * Prefetch ahead of a weight stream.  No counterpart on the pages: an
- * addition of this library, aimed at the cost the pages trace to a decode
- * step of many dependent dispatches ("epic: realize low-precision / quantized
- * performance on the OpenXLA (IREE) backend", section "The measured fusion
- * gate").
- *
- * A decode step reads the weights of its linears once each, in a fixed
- * order, and each linear waits for the previous one's output.  When all the
- * weights of the step lie in one device region in launch order, a launch can
- * ask L2 to fetch the region's bytes `distance` ahead of what it reads
- * itself, so that HBM keeps streaming while dependent launches wait for each
- * other, and later launches find their weights in L2.  The prefetch is a hint:
- * results do not depend on it.
- */
-typedef struct {
-  const void* base;   /* start of the region (device memory, 16-byte aligned) */
-  uint64_t bytes;     /* size of the region, a multiple of 16; prefetching wraps
-                         around at its end (a decode loop reads it again) */
-  uint64_t offset;    /* where this launch's weights (wq, scales, biases) start */
-  uint64_t span;      /* bytes of this launch's weights in the region, padding
-                         included; wq must lie in [offset, offset + span) */
-  uint64_t distance;  /* prefetch distance in region bytes; 0: no prefetch */
-} qlin_prefetch;
-
-/* qlin_qmv_ex with a prefetch ahead of the weight stream (pf may be NULL:
- * same as qlin_qmv_ex).  Errors as qlin_qmv_ex; a region that is misaligned,
- * not a multiple of 16 bytes, or does not hold wq where pf says returns
- * QLIN_ERR_INVALID_ARG / QLIN_ERR_MISALIGNED. */
-qlin_status qlin_qmv_prefetch(const void* x, const uint32_t* wq, const void* scales,
-                              const void* biases, void* y, int64_t M, int64_t N, int64_t K,
-                              int bits, int group_size, qlin_dtype dtype, unsigned flags,
-                              const qlin_prefetch* pf, void* stream);
-
-/*
  * A chain of dependent M = 1 products in one launch (a decode step).
  *
  * Link i computes y_i = x_i . W_hat_i^T with W_i given in the packed format

@@ -25,7 +25,7 @@ from .build_lib import LIB_PATH
 __all__ = [
     "QlinError", "lib", "quantize_affine", "dequant", "qmv", "qmm", "linear",
     "crossover_m", "device_status", "QLIN_F32", "QLIN_F16", "QLIN_BF16", "Link", "make_links",
-    "chain_workspace", "qmv_chain", "Prefetch",
+    "chain_workspace", "qmv_chain",
 ]
 
 QLIN_F32, QLIN_F16, QLIN_BF16 = 0, 1, 2
@@ -46,8 +46,6 @@ _SIGNATURES = {
                               _c_vp, _c_vp]),
     "qlin_qmv": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_qmv_ex": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [ctypes.c_uint, _c_vp]),
-    "qlin_qmv_prefetch": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 +
-                          [ctypes.c_uint, _c_vp, _c_vp]),
     "qlin_qmm": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_qmm_ex": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [ctypes.c_uint, _c_vp]),
     "qlin_linear": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
@@ -72,12 +70,6 @@ class Link(ctypes.Structure):
     _fields_ = [("wq", _c_vp), ("scales", _c_vp), ("biases", _c_vp), ("y", _c_vp),
                 ("N", _c_i64), ("K", _c_i64), ("input", ctypes.c_int32),
                 ("input_offset", ctypes.c_int32)]
-
-
-class Prefetch(ctypes.Structure):
-    """qlin_prefetch: L2 prefetch ahead of a weight stream (include/qlin.h)."""
-    _fields_ = [("base", _c_vp), ("bytes", ctypes.c_uint64), ("offset", ctypes.c_uint64),
-                ("span", ctypes.c_uint64), ("distance", ctypes.c_uint64)]
 
 
 class QlinError(RuntimeError):
@@ -184,19 +176,12 @@ def _matmul(name: str, x, wq, scales, biases, bits, group_size, out, flags=None,
     return out
 
 
-def qmv(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None, overlap_previous=False,
-        prefetch=None):
+def qmv(x, wq, scales, biases, bits, group_size=GROUP_SIZE, out=None, overlap_previous=False):
     """y = x . w_hat^T on CUDA cores (decode, small M).
 
     overlap_previous=True launches with QLIN_OVERLAP_PREVIOUS (programmatic
     dependent launch): only valid when the preceding work on the stream does
-    not write wq/scales/biases.  prefetch: a Prefetch (qlin_qmv_prefetch) that
-    places this launch's weights in a stream region and asks L2 to fetch the
-    region ahead of them."""
-    if prefetch is not None:
-        return _matmul("qlin_qmv_prefetch", x, wq, scales, biases, bits, group_size, out,
-                       flags=QLIN_OVERLAP_PREVIOUS if overlap_previous else 0,
-                       extra=(ctypes.byref(prefetch),))
+    not write wq/scales/biases."""
     if overlap_previous:
         return _matmul("qlin_qmv_ex", x, wq, scales, biases, bits, group_size, out,
                        flags=QLIN_OVERLAP_PREVIOUS)

@@ -67,8 +67,7 @@ qlin_status check_act_dtype(qlin_dtype d, const char* what) {
 
 using MatmulLauncher = qlin_status (*)(const void*, const uint32_t*, const void*, const void*,
                                        void*, int64_t, int64_t, int64_t, int, qlin_dtype,
-                                       unsigned, const Epilogue&, cudaStream_t,
-                                       const qlin_prefetch*);
+                                       unsigned, const Epilogue&, cudaStream_t);
 
 const Epilogue kPlainEpilogue = {nullptr, 0};
 
@@ -76,8 +75,7 @@ qlin_status matmul_entry(const char* name, MatmulLauncher launch, const void* x,
                          const uint32_t* wq, const void* scales, const void* biases, void* y,
                          int64_t M, int64_t N, int64_t K, int bits, int group_size,
                          qlin_dtype dtype, unsigned flags, void* stream,
-                         const Epilogue& ep = kPlainEpilogue,
-                         const qlin_prefetch* pf = nullptr) {
+                         const Epilogue& ep = kPlainEpilogue) {
   qlin_status s = check_format(N, K, bits, group_size);
   if (s != QLIN_OK) return s;
   if (flags & ~unsigned(QLIN_OVERLAP_PREVIOUS))
@@ -96,21 +94,8 @@ qlin_status matmul_entry(const char* name, MatmulLauncher launch, const void* x,
                 ep.y_f32 ? 4 : 2);
   if (ep.bias && !aligned(ep.bias, 2))
     return fail(QLIN_ERR_MISALIGNED, "%s: the layer bias must be 2-byte aligned", name);
-  if (pf && pf->distance) {
-    if (!pf->base || !aligned(pf->base, 16) || pf->bytes % 16)
-      return fail(QLIN_ERR_MISALIGNED,
-                  "%s: the prefetch region must start 16-byte aligned and be a multiple of 16 "
-                  "bytes", name);
-    const uint64_t wq_bytes = uint64_t(N) * uint64_t(K) * uint64_t(bits) / 8;
-    const uintptr_t b = reinterpret_cast<uintptr_t>(pf->base);
-    const uintptr_t w = reinterpret_cast<uintptr_t>(wq);
-    if (pf->offset > pf->bytes || pf->span > pf->bytes - pf->offset || pf->span < wq_bytes ||
-        w < b + pf->offset || w - (b + pf->offset) > pf->span - wq_bytes)
-      return fail(QLIN_ERR_INVALID_ARG,
-                  "%s: wq does not lie in [offset, offset + span) of the prefetch region", name);
-  }
   return launch(x, wq, scales, biases, y, M, N, K, bits, dtype, flags, ep,
-                reinterpret_cast<cudaStream_t>(stream), pf);
+                reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -189,15 +174,6 @@ qlin_status qlin_qmv_ex(const void* x, const uint32_t* wq, const void* scales, c
   g_last_error[0] = 0;
   return matmul_entry("qlin_qmv_ex", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
                       group_size, dtype, flags, stream);
-}
-
-qlin_status qlin_qmv_prefetch(const void* x, const uint32_t* wq, const void* scales,
-                              const void* biases, void* y, int64_t M, int64_t N, int64_t K,
-                              int bits, int group_size, qlin_dtype dtype, unsigned flags,
-                              const qlin_prefetch* pf, void* stream) {
-  g_last_error[0] = 0;
-  return matmul_entry("qlin_qmv_prefetch", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
-                      group_size, dtype, flags, stream, kPlainEpilogue, pf);
 }
 
 qlin_status qlin_qmm_ex(const void* x, const uint32_t* wq, const void* scales,

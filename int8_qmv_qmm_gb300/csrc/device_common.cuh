@@ -36,13 +36,6 @@ struct Act<__nv_bfloat16> {
 
 __device__ __forceinline__ float u32_as_f32(uint32_t v) { return __uint_as_float(v); }
 
-// Asks L2 to fetch [p, p + bytes) (p and bytes multiples of 16); no data
-// comes back to the SM.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  if (bytes)
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Programmatic dependent launch: wait until the preceding kernel on the stream
 // has completed and its writes are visible (returns at once when the launch
 // has no programmatic dependency), and allow the next kernel to launch early.

@@ -33,12 +33,10 @@ struct Epilogue {
 
 qlin_status launch_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, const Epilogue& ep, cudaStream_t st,
-                       const qlin_prefetch* pf = nullptr);
+                       unsigned flags, const Epilogue& ep, cudaStream_t st);
 qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, const Epilogue& ep, cudaStream_t st,
-                       const qlin_prefetch* pf = nullptr);  // pf: ignored
+                       unsigned flags, const Epilogue& ep, cudaStream_t st);
 
 // Limits of the chain kernel's waits for an input link.  stalled_link >= 0
 // (tests only) makes the readers of that link wait for one row block more

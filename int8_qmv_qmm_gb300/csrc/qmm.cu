@@ -1021,8 +1021,7 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
 
 qlin_status launch_qmm(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, const Epilogue& ep, cudaStream_t st,
-                       const qlin_prefetch*) {
+                       unsigned flags, const Epilogue& ep, cudaStream_t st) {
   if (dtype == QLIN_F16)
     return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, ep, flags, st)
                      : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, ep, flags, st);

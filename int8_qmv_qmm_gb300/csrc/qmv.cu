@@ -57,33 +57,7 @@ struct Shape {
   int stage_bytes;  // bytes of one stage (weights, then scales and biases)
   unsigned flags;
   Epilogue ep;      // layer bias and f32 output (qlin_linear_ex)
-  // L2 prefetch ahead of the weight stream (qlin_qmv_prefetch); pf_base null: none
-  const uint8_t* pf_base;
-  unsigned long long pf_bytes;   // size of the stream region (the prefetch wraps at its end)
-  unsigned long long pf_offset;  // this launch's first weight byte in the region
-  unsigned long long pf_dist;    // prefetch distance in stream bytes
-  unsigned long long pf_ratio;   // stream bytes per packed-code byte, 16.16 fixed point
 };
-
-// Prefetch into L2 the stream bytes `pf_dist` ahead of the packed-code bytes
-// [off, off + bytes) of this launch (offsets within wq).  Packed-code offsets
-// are scaled by pf_ratio so that the launches' scales and biases, which sit
-// between the packed codes of consecutive launches in the stream, are covered
-// too.  Start rounded down and end rounded up to 16 bytes.
-__device__ __forceinline__ void prefetch_ahead(const Shape& sh, unsigned long long off,
-                                               unsigned bytes) {
-  unsigned long long a = sh.pf_offset + ((off * sh.pf_ratio) >> 16) + sh.pf_dist;
-  unsigned long long n = (((unsigned long long)bytes * sh.pf_ratio) >> 16) + 16;
-  a %= sh.pf_bytes;
-  a &= ~15ull;
-  n = (n + 15) & ~15ull;
-  while (n) {
-    const unsigned long long piece = min(n, sh.pf_bytes - a);
-    prefetch_l2(sh.pf_base + a, unsigned(piece));
-    n -= piece;
-    a = 0;
-  }
-}
 
 // MODE 0: generic k-tiles, scales read from global memory; 1: generic k-tiles,
 // scales copied into the stage; 2: fixed 2048-code k-tiles with scales copied
@@ -156,8 +130,6 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
           if (lane == 0) {
             bulk_copy(stage, reinterpret_cast<const uint8_t*>(wq) + int64_t(row0) * row_bytes,
                       uint32_t(nr) * w_bytes, full0 + 8u * s);
-            if (sh.pf_base)
-              prefetch_ahead(sh, (unsigned long long)row0 * row_bytes, uint32_t(nr) * w_bytes);
             if constexpr (kScaleCopy) {
               const int64_t g0 = int64_t(row0) * gpr;
               bulk_copy(sb0, scales + g0, uint32_t(nr) * sb_bytes, full0 + 8u * s);
@@ -172,10 +144,6 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
                       reinterpret_cast<const uint8_t*>(wq) + row * row_bytes +
                           int64_t(kt) * sh.kt_bytes,
                       w_bytes, full0 + 8u * s);
-            if (sh.pf_base)
-              prefetch_ahead(sh, (unsigned long long)row * row_bytes +
-                                     (unsigned long long)kt * sh.kt_bytes,
-                             w_bytes);
             if constexpr (kScaleCopy) {
               const int64_t g0 = row * gpr + int64_t(kt) * kt_groups;
               bulk_copy(sb0 + uint32_t(r) * sb_bytes, scales + g0, sb_bytes, full0 + 8u * s);
@@ -392,25 +360,13 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
 #undef QLIN_QMV_LAUNCH
 }
 
-struct Prefetch {
-  const qlin_prefetch* pf;  // null: no prefetch
-  uint64_t wq_bytes;        // packed-code bytes of this launch
-};
-
 template <int BITS, typename AT>
 qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                      void* y, int64_t M, int64_t N, int64_t K, unsigned flags,
-                     const Epilogue& ep, const Prefetch& p, cudaStream_t st) {
+                     const Epilogue& ep, cudaStream_t st) {
   Shape sh{};
   sh.flags = flags;
   sh.ep = ep;
-  if (p.pf && p.pf->distance) {
-    sh.pf_base = static_cast<const uint8_t*>(p.pf->base);
-    sh.pf_bytes = p.pf->bytes;
-    sh.pf_offset = p.pf->offset;
-    sh.pf_dist = p.pf->distance;
-    sh.pf_ratio = (p.pf->span << 16) / p.wq_bytes;
-  }
   sh.M = int(M);
   sh.N = int(N);
   sh.K = int(K);
@@ -428,16 +384,13 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
 
 qlin_status launch_qmv(const void* x, const uint32_t* wq, const void* scales, const void* biases,
                        void* y, int64_t M, int64_t N, int64_t K, int bits, qlin_dtype dtype,
-                       unsigned flags, const Epilogue& ep, cudaStream_t st,
-                       const qlin_prefetch* pf) {
-  Prefetch p{};
-  if (pf) p = {pf, uint64_t(N) * uint64_t(K) * uint64_t(bits) / 8};
+                       unsigned flags, const Epilogue& ep, cudaStream_t st) {
   if (dtype == QLIN_F16)
-    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, flags, ep, p, st)
-                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, flags, ep, p, st);
-  return bits == 4
-             ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, ep, p, st)
-             : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, ep, p, st);
+    return bits == 4 ? dispatch<4, __half>(x, wq, scales, biases, y, M, N, K, flags, ep, st)
+                     : dispatch<8, __half>(x, wq, scales, biases, y, M, N, K, flags, ep, st);
+  return bits == 4 ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, ep, st)
+                   : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, ep,
+                                                st);
 }
 
 cudaError_t qmv_take_device_status(unsigned* flags) {

@@ -27,7 +27,7 @@ from __future__ import annotations
 
 import torch
 
-from . import Prefetch, chain_workspace, dequant, make_links, qmv, qmv_chain, quantize_affine
+from . import chain_workspace, dequant, make_links, qmv, qmv_chain, quantize_affine
 from . import synthetic as S
 
 _FUSED = (("qkv", ("q_proj", "k_proj", "v_proj")), ("o", ("o_proj",)),
@@ -41,22 +41,18 @@ def _round_up(v: int, a: int = 256) -> int:
 class DecodeStep:
     def __init__(self, device, bits: int = 8, dtype: torch.dtype = torch.float16,
                  seed: int = 2, layers: int = S.LLAMA_1B_LAYERS, lm_head: bool = True,
-                 overlap: bool = True, mode: str = "launches", prefetch_distance: int = 0):
+                 overlap: bool = True, mode: str = "launches"):
         """mode "launches": one qlin_qmv launch per fused linear (overlapped
         with programmatic dependent launch when ``overlap``; the faster mode on
         GB300); mode "chain": the whole step is one qlin_qmv_chain launch.
 
         All packed weights, scales and biases live in one device region, in
-        launch order (each piece 256-byte aligned).  prefetch_distance > 0
-        makes every launch ask L2 for the region's bytes that far ahead of
-        what it reads itself (qlin_qmv_prefetch), so that HBM keeps streaming
-        while the dependent launches wait for each other."""
+        launch order (each piece 256-byte aligned)."""
         self.device = torch.device(device)
         self.bits = bits
         self.dtype = dtype
         self.overlap = overlap
         self.mode = mode
-        self.prefetch_distance = int(prefetch_distance)
         shapes = {name: (n, k) for name, n, k in S.LLAMA_1B_LINEARS}
         # original linears, in the order of the weight seeds:
         # (name, layer, N, K, unit index, first row in the unit, weight seed)
@@ -108,18 +104,7 @@ class DecodeStep:
         hidden = S.LLAMA_1B_LINEARS[0][2]
         self.x0 = torch.zeros((1, hidden), dtype=dtype, device=self.device)
         self.graph = None
-        self._set_prefetch()
         self._build_chain()
-
-    def _set_prefetch(self):
-        self._prefetch = [None if self.prefetch_distance <= 0 else
-                          Prefetch(self.region.data_ptr(), self.region.numel(), u["offset"],
-                                   u["span"], self.prefetch_distance) for u in self.units]
-
-    def set_prefetch_distance(self, distance: int):
-        """Change the prefetch distance (recapture the graph afterwards)."""
-        self.prefetch_distance = int(distance)
-        self._set_prefetch()
 
     def _build_chain(self):
         """The link table of the step (same chaining as input_of)."""
@@ -175,8 +160,7 @@ class DecodeStep:
                overlap: bool = False):
         d = self.units[u]
         return qmv(x, d["wq"], d["scales"], d["biases"], self.bits,
-                   out=d["out"] if out is None else out, overlap_previous=overlap,
-                   prefetch=self._prefetch[u])
+                   out=d["out"] if out is None else out, overlap_previous=overlap)
 
     def launch_chain(self):
         qmv_chain(self.x0, self._links, len(self.units), self.bits, self.dtype, self._workspace)
