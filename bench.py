@@ -432,47 +432,52 @@ def time_qmm(q, device, peaks, reps: int = 100, warm: int = 10):
 
 
 def crossover_sweep(q, device, reps: int = 100, warm: int = 10):
-    """qmv vs qmm on the batched-decode sweep (M = 1..32, 4-bit, bf16), L2
-    flushed between timed launches; the crossover is the smallest M from which
-    qmm is faster on every shape."""
+    """qmv vs qmm on the batched-decode sweep (M = 1..32, 4-bit, bf16 as the
+    workload has it, and f16), L2 flushed between timed launches; per dtype the
+    crossover is the smallest M from which qmm is at least as fast on every
+    shape, next to the library's choice."""
     import torch
 
     from int8_qmv_qmm_gb300 import synthetic as S
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
-    table = []
-    for (n, k) in ((8192, 2048), (2048, 8192)):
-        w = torch.from_numpy(S.weights_f32(S.weight_seed(3, n), n, k)).to(device)
-        wq, sc, bi = q.quantize_affine(w, 4, sdtype=torch.bfloat16)
-        del w
+    out = {}
+    for dt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        table = []
+        for (n, k) in ((8192, 2048), (2048, 8192)):
+            w = torch.from_numpy(S.weights_f32(S.weight_seed(3, n), n, k)).to(device)
+            wq, sc, bi = q.quantize_affine(w, 4, sdtype=tdt)
+            del w
+            for m in (1, 2, 4, 8, 16, 32):
+                x = S.activations(3, m, k, dt).to(device)
+                y = torch.empty((m, n), dtype=tdt, device=device)
+                row = {"n": n, "k": k, "m": m}
+                for name in ("qmv", "qmm"):
+                    fn = getattr(q, name)
+                    for _ in range(warm):
+                        fn(x, wq, sc, bi, 4, out=y)
+                    ts = []
+                    for _ in range(reps):
+                        flush_l2(flush)
+                        torch.cuda._sleep(100000)  # the host enqueues the events and launch meanwhile
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        fn(x, wq, sc, bi, 4, out=y)
+                        e1.record(stream)
+                        e1.synchronize()
+                        ts.append(e0.elapsed_time(e1) * 1e3)
+                    row[name + "_us"] = statistics.median(ts)
+                row["packed_gbs_qmv"] = (wq.numel() * 4 + 2 * sc.numel() * 2) / row["qmv_us"] / 1e3
+                row["library_picks"] = "qmm" if m >= q.crossover_m(n, k, 4, tdt) else "qmv"
+                table.append(row)
+        cross = None
         for m in (1, 2, 4, 8, 16, 32):
-            x = S.activations(3, m, k, "bf16").to(device)
-            y = torch.empty((m, n), dtype=torch.bfloat16, device=device)
-            row = {"n": n, "k": k, "m": m}
-            for name in ("qmv", "qmm"):
-                fn = getattr(q, name)
-                for _ in range(warm):
-                    fn(x, wq, sc, bi, 4, out=y)
-                ts = []
-                for _ in range(reps):
-                    flush_l2(flush)
-                    torch.cuda._sleep(100000)  # the host enqueues the events and launch meanwhile
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    fn(x, wq, sc, bi, 4, out=y)
-                    e1.record(stream)
-                    e1.synchronize()
-                    ts.append(e0.elapsed_time(e1) * 1e3)
-                row[name + "_us"] = statistics.median(ts)
-            row["packed_gbs_qmv"] = (wq.numel() * 4 + 2 * sc.numel() * 2) / row["qmv_us"] / 1e3
-            table.append(row)
-    cross = None
-    for m in (1, 2, 4, 8, 16, 32):
-        if all(r["qmm_us"] <= r["qmv_us"] for r in table if r["m"] == m):
-            cross = m
-            break
-    return {"crossover_m": cross, "table": table}
+            if all(r["qmm_us"] <= r["qmv_us"] for r in table if r["m"] == m):
+                cross = m
+                break
+        out[dt] = {"crossover_m": cross, "table": table}
+    return out
 
 
 def time_flushed(fn, device, flush, reps: int = 100, warm: int = 10):

@@ -253,7 +253,8 @@ qlin_status qlin_qmm_ex(const void* x, const uint32_t* wq, const void* scales, c
                         qlin_dtype dtype, unsigned flags, void* stream);
 
 /*
- * Dispatch to qlin_qmv when M < qlin_crossover_m(N, K, bits), else qlin_qmm.
+ * Dispatch to qlin_qmv when M < qlin_crossover_m_dtype(N, K, bits, dtype), else
+ * qlin_qmm.
  * The product is the one both kernels define (same passages); choosing
  * between them by M is an addition of this library.
  */
@@ -261,10 +262,14 @@ qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
                         const void* biases, void* y, int64_t M, int64_t N, int64_t K, int bits,
                         int group_size, qlin_dtype dtype, void* stream);
 
-/* Smallest M for which qlin_linear picks the tensor-core path, from
- * measurements on GB300; the environment variable QLIN_CROSSOVER_M (read once
+/* Smallest M for which qlin_linear picks the tensor-core path for activation
+ * dtype `dtype`, from measurements on GB300 (8 for bf16; for f16 8 when
+ * N >= K, 4 when K > N); the environment variable QLIN_CROSSOVER_M (read once
  * per process) overrides it.  No counterpart on the pages: an addition of
  * this library. */
+int64_t qlin_crossover_m_dtype(int64_t N, int64_t K, int bits, qlin_dtype dtype);
+
+/* qlin_crossover_m_dtype for f16 activations. */
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits);
 
 /*

@@ -51,6 +51,7 @@ _SIGNATURES = {
     "qlin_linear": (_c_int, [_c_vp] * 5 + [_c_i64] * 3 + [_c_int] * 3 + [_c_vp]),
     "qlin_linear_ex": (_c_int, [_c_vp] * 6 + [_c_i64] * 3 + [_c_int] * 4 + [_c_vp]),
     "qlin_crossover_m": (_c_i64, [_c_i64, _c_i64, _c_int]),
+    "qlin_crossover_m_dtype": (_c_i64, [_c_i64, _c_i64, _c_int, _c_int]),
     "qlin_qmv_chain_workspace_size": (ctypes.c_size_t, [_c_int]),
     "qlin_qmv_chain": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int, _c_vp,
                                 ctypes.c_size_t, _c_vp]),
@@ -259,8 +260,9 @@ def qmv_chain(x0, link_array, n_links, bits, dtype, workspace, group_size=GROUP_
                                 ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)))
 
 
-def crossover_m(n: int, k: int, bits: int) -> int:
-    return int(lib().qlin_crossover_m(n, k, bits))
+def crossover_m(n: int, k: int, bits: int, dtype: torch.dtype = torch.float16) -> int:
+    """Smallest M for which linear() takes the tensor-core kernel."""
+    return int(lib().qlin_crossover_m_dtype(n, k, bits, _DTYPE_CODE[dtype]))
 
 
 def device_status() -> int:

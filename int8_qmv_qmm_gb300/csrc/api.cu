@@ -281,7 +281,7 @@ qlin_status qlin_testing_qmv_chain_stalled(const void* x0, const qlin_link* link
                      stream);
 }
 
-int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
+int64_t qlin_crossover_m_dtype(int64_t N, int64_t K, int bits, qlin_dtype dtype) {
   (void)bits;
   // QLIN_CROSSOVER_M (a positive integer) overrides the measured choice; read
   // once, on the first call
@@ -291,18 +291,25 @@ int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
     return v >= 1 ? v : 0;
   }();
   if (env_m) return env_m;
-  // Measured on GB300 (batched-decode sweep, 4-bit, bf16, L2 flushed): the
-  // tensor-core kernel (wide token tiles, K split over a cluster) overtakes
-  // the CUDA-core one at M = 8 when N >= K (8192 x 2048: 16.4 vs 20.5 us) and
-  // at M = 4 when K > N (2048 x 8192: 22.5 vs 24.6 us).
+  // Measured on GB300 (batched-decode sweep, L2 flushed, 4- and 8-bit alike):
+  // with f16 the tensor-core kernel overtakes the CUDA-core one at M = 8 when
+  // N >= K (8192 x 2048: 16.4 vs 20.5 us) and at M = 4 when K > N (2048 x 8192:
+  // 22.5 vs 22.5 us); bf16 issues two MMAs per K step (the residual operand)
+  // and overtakes at M = 8 on both shapes (2048 x 8192 at M = 4: 28.7 vs
+  // 24.6 us, at M = 8: 28.7 vs 34.8 us).
+  if (dtype == QLIN_BF16) return 8;
   return K > N ? 4 : 8;
+}
+
+int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {
+  return qlin_crossover_m_dtype(N, K, bits, QLIN_F16);
 }
 
 qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
                         const void* biases, void* y, int64_t M, int64_t N, int64_t K, int bits,
                         int group_size, qlin_dtype dtype, void* stream) {
   g_last_error[0] = 0;
-  if (M < qlin_crossover_m(N, K, bits))
+  if (M < qlin_crossover_m_dtype(N, K, bits, dtype))
     return matmul_entry("qlin_linear", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
                         group_size, dtype, 0u, stream);
   return matmul_entry("qlin_linear", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,
@@ -319,7 +326,7 @@ qlin_status qlin_linear_ex(const void* x, const uint32_t* wq, const void* scales
                 "qlin_linear_ex: y dtype %d must be float32 or the activation dtype %d",
                 int(y_dtype), int(dtype));
   const Epilogue ep = {layer_bias, y_dtype == QLIN_F32 ? 1 : 0};
-  if (M < qlin_crossover_m(N, K, bits))
+  if (M < qlin_crossover_m_dtype(N, K, bits, dtype))
     return matmul_entry("qlin_linear_ex", launch_qmv, x, wq, scales, biases, y, M, N, K, bits,
                         group_size, dtype, 0u, stream, ep);
   return matmul_entry("qlin_linear_ex", launch_qmm, x, wq, scales, biases, y, M, N, K, bits,

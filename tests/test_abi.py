@@ -156,3 +156,11 @@ def test_testing_chain_entry_validation(L):
     assert call(1, 1000) == INVALID       # nothing reads the last link
     assert call(0, 0) == INVALID          # limit out of range
     assert call(0, 3000000) == INVALID
+
+
+def test_crossover_by_dtype(L):
+    """bf16 issues two MMAs per K step, so it switches to the tensor cores later."""
+    assert L.qlin_crossover_m_dtype(2048, 8192, 4, q.QLIN_F16) == 4
+    assert L.qlin_crossover_m_dtype(2048, 8192, 4, q.QLIN_BF16) == 8
+    assert L.qlin_crossover_m_dtype(8192, 2048, 8, q.QLIN_BF16) == 8
+    assert L.qlin_crossover_m(2048, 8192, 4) == L.qlin_crossover_m_dtype(2048, 8192, 4, q.QLIN_F16)

@@ -195,6 +195,7 @@ def test_one_hot_rows_reproduce_dequant_bit_exactly(dev, fn, bits, dt):
 def test_linear_dispatches_both_paths(dev):
     n, k, bits, dt = 300, 512, 4, "f16"
     assert q.crossover_m(8192, 2048, 4) == 8 and q.crossover_m(2048, 8192, 4) == 4
+    assert q.crossover_m(2048, 8192, 8, torch.bfloat16) == 8
     for m in (1, 40):
         w, x, ref = case(5 + m, m, n, k, bits, dt)
         wq, sc, bi = _upload(dev, w, bits, dt)
@@ -290,7 +291,7 @@ def test_groups_of_near_zero_weights(dev, fn, bits, dt):
     ref = O.linear_ref(x.double().numpy(), w, bits, 64, dt)
     wq, sc, bi = _upload(dev, w, bits, dt)
     xd = x.to(dev)
-    assert (m >= q.crossover_m(n, k, bits)) == (fn == "qmm")   # linear picks fn
+    assert (m >= q.crossover_m(n, k, bits, TORCH_DT[dt])) == (fn == "qmm")   # linear picks fn
     y32 = q.linear(xd, wq, sc, bi, bits, out_dtype=torch.float32)
     assert_within_tolerance(y32, ref, f"near-zero groups {fn} b={bits} {dt} f32 out")
     y = getattr(q, fn)(xd, wq, sc, bi, bits)
