@@ -864,8 +864,13 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
   // (kDequantGroups + 2) barriers per stage (at most 8), two pairs of
   // accumulator barriers, the teardown barrier and the TMEM address slot
   static_assert((kDequantGroups + 2) * 8 * 8 + 4 * 8 + 8 + 8 + 4 <= kBarBytes, "barrier block");
-  const int stages =
+  int stages =
       std::min(std::min(8, L::kMaxStages), (kMaxSmem - 1024 - kBarBytes) / L::kStageBytes);
+  // QLIN_QMM_STAGES (2..8) caps the ring depth, for tuning
+  if (const char* env = std::getenv("QLIN_QMM_STAGES")) {
+    const int v = std::atoi(env);
+    if (v >= 2 && v < stages) stages = v;
+  }
   if (stages < 2) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: tile does not fit");
   // split-K: slices of at least 16 columns, and the receive buffer of the
   // reduction fits in the ring
