@@ -320,6 +320,76 @@ __device__ __forceinline__ uint32_t splat(AT v) {
   return uint32_t(u) | (uint32_t(u) << 16);
 }
 
+// The 64 reconstructed weights of row r of a stage's packed tile (two per
+// register, k ascending) and, for bfloat16, their residuals (lo_pair): the
+// reconstruction of qlin_dequant, bit for bit.  Rows past N (row_ok false)
+// give zeros.
+template <int BITS, typename AT, int kSplit>
+__device__ __forceinline__ void dequant_row(const uint8_t* wrow, int r, AT sc, AT bc, bool row_ok,
+                                            uint32_t (&a)[32], uint32_t (&lo)[kSplit == 2 ? 32 : 1]) {
+  const uint32_t s2 = row_ok ? splat(sc) : 0u, b2 = row_ok ? splat(bc) : 0u;
+  if constexpr (kSplit == 2) {
+    const float sv = row_ok ? Act<AT>::to_f32(sc) : 0.0f;
+    const float bv = row_ok ? Act<AT>::to_f32(bc) : 0.0f;
+    const float2 sf = make_float2(sv, sv), bf = make_float2(bv, bv);
+    if constexpr (BITS == 4) {
+      const int sw = (r >> 2) & 1;
+      const uint4 v0 = *reinterpret_cast<const uint4*>(wrow + ((0 ^ sw) << 4));
+      const uint4 v1 = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
+      const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        dequant_word4_split(words[c], s2, b2, sf, bf,
+                            *reinterpret_cast<uint32_t(*)[4]>(a + 4 * c),
+                            *reinterpret_cast<uint32_t(*)[4]>(lo + 4 * c));
+    } else {
+      const int sw = (r >> 1) & 3;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ sw) << 4));
+        const uint32_t ws4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dequant_word8_split(ws4[e], s2, b2, sf, bf, a[8 * c + 2 * e], a[8 * c + 2 * e + 1],
+                              lo[8 * c + 2 * e], lo[8 * c + 2 * e + 1]);
+      }
+    }
+  } else if constexpr (BITS == 4) {
+    // packed rows are 32 bytes in the 32-byte TMA swizzle: chunk c of row
+    // r sits at chunk c ^ ((r >> 2) & 1)
+    const int sw = (r >> 2) & 1;
+    const uint4 v0 = *reinterpret_cast<const uint4*>(wrow + ((0 ^ sw) << 4));
+    const uint4 v1 = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
+    const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 o = dequant_word4<AT>(words[c], s2, b2);
+      a[4 * c] = o.x;
+      a[4 * c + 1] = o.y;
+      a[4 * c + 2] = o.z;
+      a[4 * c + 3] = o.w;
+    }
+  } else {
+    // packed rows are 64 bytes in the 64-byte TMA swizzle: chunk c of row
+    // r sits at chunk c ^ ((r >> 1) & 3)
+    const int sw = (r >> 1) & 3;
+    uint32_t words[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ sw) << 4));
+      words[4 * c] = v.x;
+      words[4 * c + 1] = v.y;
+      words[4 * c + 2] = v.z;
+      words[4 * c + 3] = v.w;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      dequant_word8<AT>(words[2 * c], s2, b2, a[4 * c], a[4 * c + 1]);
+      dequant_word8<AT>(words[2 * c + 1], s2, b2, a[4 * c + 2], a[4 * c + 3]);
+    }
+  }
+}
+
 template <int BITS, typename AT, int BN, bool SCALE_TMA>
 __global__ void __launch_bounds__(kThreads, 1)
     qmm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -538,72 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           sc = ss[r * 8 + (kb & 7)];
           bc = ss[kBM * 8 + r * 8 + (kb & 7)];
         }
-        const uint32_t s2 = row_ok ? splat(sc) : 0u, b2 = row_ok ? splat(bc) : 0u;
         const uint8_t* wrow = gbase + (w_addr(cs) - base) + r * G::kPackedRowBytes;
         // the row's 64 reconstructed weights, two per register, k ascending
         // (and, for bfloat16, their residuals)
         uint32_t a[32];
         uint32_t lo[kSplit == 2 ? 32 : 1];
-        if constexpr (kSplit == 2) {
-          const float sv = row_ok ? Act<AT>::to_f32(sc) : 0.0f;
-          const float bv = row_ok ? Act<AT>::to_f32(bc) : 0.0f;
-          const float2 sf = make_float2(sv, sv), bf = make_float2(bv, bv);
-          if constexpr (BITS == 4) {
-            const int sw = (r >> 2) & 1;
-            const uint4 v0 = *reinterpret_cast<const uint4*>(wrow + ((0 ^ sw) << 4));
-            const uint4 v1 = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
-            const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              dequant_word4_split(words[c], s2, b2, sf, bf,
-                                  *reinterpret_cast<uint32_t(*)[4]>(a + 4 * c),
-                                  *reinterpret_cast<uint32_t(*)[4]>(lo + 4 * c));
-          } else {
-            const int sw = (r >> 1) & 3;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ sw) << 4));
-              const uint32_t ws4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                dequant_word8_split(ws4[e], s2, b2, sf, bf, a[8 * c + 2 * e], a[8 * c + 2 * e + 1],
-                                    lo[8 * c + 2 * e], lo[8 * c + 2 * e + 1]);
-            }
-          }
-        } else if constexpr (BITS == 4) {
-          // packed rows are 32 bytes in the 32-byte TMA swizzle: chunk c of row
-          // r sits at chunk c ^ ((r >> 2) & 1)
-          const int sw = (r >> 2) & 1;
-          const uint4 lo = *reinterpret_cast<const uint4*>(wrow + ((0 ^ sw) << 4));
-          const uint4 hi = *reinterpret_cast<const uint4*>(wrow + ((1 ^ sw) << 4));
-          const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 o = dequant_word4<AT>(words[c], s2, b2);
-            a[4 * c] = o.x;
-            a[4 * c + 1] = o.y;
-            a[4 * c + 2] = o.z;
-            a[4 * c + 3] = o.w;
-          }
-        } else {
-          // packed rows are 64 bytes in the 64-byte TMA swizzle: chunk c of row
-          // r sits at chunk c ^ ((r >> 1) & 3)
-          const int sw = (r >> 1) & 3;
-          uint32_t words[16];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((c ^ sw) << 4));
-            words[4 * c] = v.x;
-            words[4 * c + 1] = v.y;
-            words[4 * c + 2] = v.z;
-            words[4 * c + 3] = v.w;
-          }
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            dequant_word8<AT>(words[2 * c], s2, b2, a[4 * c], a[4 * c + 1]);
-            dequant_word8<AT>(words[2 * c + 1], s2, b2, a[4 * c + 2], a[4 * c + 3]);
-          }
-        }
+        dequant_row<BITS, AT, kSplit>(wrow, r, sc, bc, row_ok, a, lo);
         // into the stage's A slot; complete before the MMA issuer is told
         tmem_st_32x32b_x32(a_lane + uint32_t(cs * L::kAColsPerStage), a);
         if constexpr (kSplit == 2)
