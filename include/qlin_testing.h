@@ -1,8 +1,8 @@
 /*
- * qlin_testing.h -- entry points of libqlin that exist only so that the
- * library's own tests can reach failure paths without faulting or hanging a
- * GPU.  They have no counterpart on the pages the method comes from, and no
- * product code calls them.
+ * qlin_testing.h -- entry points of libqlin that exist only for the library's
+ * own tests: to reach failure paths without faulting or hanging a GPU, and to
+ * check host-side launch choices without one.  They have no counterpart on
+ * the pages the method comes from, and no product code calls them.
  */
 #ifndef QLIN_TESTING_H_
 #define QLIN_TESTING_H_
@@ -30,6 +30,18 @@ qlin_status qlin_testing_qmv_chain_stalled(const void* x0, const qlin_link* link
                                            void* workspace, size_t workspace_bytes,
                                            int stalled_link, unsigned wait_limit_us,
                                            void* stream);
+
+/*
+ * The split of K that qlin_qmv (and qlin_linear's qmv path) would use for an
+ * N x K matrix of `bits`-bit codes on a device with `sm_count` SMs: the
+ * number of CTAs (a thread-block cluster) that share each row block, each
+ * taking an equal share of the row's k-tiles (1: no split).  Host logic only;
+ * touches no device.  Honours the QLIN_QMV_SPLIT and QLIN_QMV_R tuning
+ * variables as the launcher does.  Returns -1 for arguments qlin_qmv would
+ * reject (bits not 4 or 8, K not a positive multiple of 64, N < 1) or
+ * sm_count < 1.
+ */
+int qlin_testing_qmv_split(int64_t N, int64_t K, int bits, int sm_count);
 
 #ifdef __cplusplus
 }

@@ -57,10 +57,12 @@ _SIGNATURES = {
                                 ctypes.c_size_t, _c_vp]),
     "qlin_qmv_chain_static": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int, _c_vp]),
     "qlin_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
-    # include/qlin_testing.h: failure paths for the library's own tests
+    # include/qlin_testing.h: failure paths and host-side choices, for the
+    # library's own tests
     "qlin_testing_qmv_chain_stalled": (_c_int, [_c_vp, _c_vp, _c_int, _c_int, _c_int, _c_int,
                                                 _c_vp, ctypes.c_size_t, _c_int, ctypes.c_uint,
                                                 _c_vp]),
+    "qlin_testing_qmv_split": (_c_int, [_c_i64, _c_i64, _c_int, _c_int]),
 }
 
 _LIB = None

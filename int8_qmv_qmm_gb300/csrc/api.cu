@@ -258,6 +258,11 @@ qlin_status qlin_qmv_chain(const void* x0, const qlin_link* links, int n_links, 
                      kDefaultChainWaits, stream);
 }
 
+int qlin_testing_qmv_split(int64_t N, int64_t K, int bits, int sm_count) {
+  if ((bits != 4 && bits != 8) || K < 64 || K % 64 != 0 || N < 1 || sm_count < 1) return -1;
+  return qlin::qmv_plan_split(N, K, bits, sm_count);
+}
+
 qlin_status qlin_testing_qmv_chain_stalled(const void* x0, const qlin_link* links, int n_links,
                                            int bits, int group_size, qlin_dtype dtype,
                                            void* workspace, size_t workspace_bytes,

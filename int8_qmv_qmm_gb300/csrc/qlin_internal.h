@@ -52,6 +52,10 @@ qlin_status launch_qmv_chain(const void* x0, const qlin_link* links, int n_links
                              cudaStream_t st);
 int chain_max_links();
 
+// The number of CTAs qlin_qmv gives each row block (its split of K) for an
+// N x K matrix of `bits`-bit codes on a device with `sms` SMs.
+int qmv_plan_split(int64_t N, int64_t K, int bits, int sms);
+
 // Read and clear the kernels' device status words (no synchronisation).
 cudaError_t qmm_take_device_status(unsigned* flags);
 cudaError_t qmv_take_device_status(unsigned* flags);

@@ -280,28 +280,7 @@ __device__ __forceinline__ void dequant_word8_split(uint32_t w, uint32_t s2, uin
   l1 = lo_pair(make_float2(f[2], f[3]), sf, bf, h1);
 }
 
-// ---- thread-block cluster helpers (split-K reduction)
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster; release/acquire orders the
-// shared::cluster stores made before it with the loads made after it.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// The address of this CTA's shared-memory location `addr` in CTA `rank`.
-__device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
+// ---- split-K reduction
 // Asynchronous 16-byte store into another CTA's shared memory; its bytes are
 // counted (complete_tx) on that CTA's mbarrier `bar` (a shared::cluster
 // address too).
@@ -413,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // split  > 1: a cluster of `split` CTAs shares one tile (grid = tiles x
   // split), CTA `rank` taking k-blocks [kb0, kb1); the partial accumulators
   // are summed through distributed shared memory at the end.
-  const int rank = split > 1 ? int(cluster_ctarank()) : 0;
+  const int rank = split > 1 ? int(ptx::cluster_ctarank()) : 0;
   const int t_first = int(blockIdx.x) / split, t_step = int(gridDim.x) / split;
   const int kb0 = rank * kb_count / split, kb1 = (rank + 1) * kb_count / split;
 
@@ -698,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // before any of them can start (the cluster barrier below)
     if (threadIdx.x == 0 && t_first < total_tiles)
       ptx::mbar_arrive_expect_tx(red_bar, uint32_t((split - 1) * slice * kBM * 4));
-    cluster_sync();  // every CTA of the cluster is past its K loop and armed
+    ptx::cluster_sync();  // every CTA of the cluster is past its K loop and armed
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16);
@@ -710,8 +689,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (d == rank) continue;
         const int slot = rank < d ? rank : rank - 1;
         const uint32_t dst =
-            map_shared_rank(base, uint32_t(d)) + uint32_t(slot * (slice / 4) * kBM * 16);
-        const uint32_t dst_bar = map_shared_rank(red_bar, uint32_t(d));
+            ptx::map_shared_rank(base, uint32_t(d)) + uint32_t(slot * (slice / 4) * kBM * 16);
+        const uint32_t dst_bar = ptx::map_shared_rank(red_bar, uint32_t(d));
 #pragma unroll 1
         for (int c0 = 0; c0 < slice; c0 += batch) {
           uint32_t v[kRBatch];
@@ -815,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // no CTA leaves while another may still be writing into it
-    cluster_sync();
+    ptx::cluster_sync();
     ptx::tc_fence_before();
     __syncthreads();
   }

@@ -49,10 +49,13 @@ constexpr int kProducerWarp = kConsumerWarps;
 struct Shape {
   int M, N, K;
   int C;            // 16-byte chunks per row
-  int rounds;       // ceil(C / 32): rounds of the lane-transposed x layout
+  int rounds;       // rounds of the lane-transposed x layout of one CTA's
+                    // k range: ceil(C / split / 32)
   int kt_bytes;     // bytes of one row per k-tile (multiple of 16, divides the row)
   int n_kt;         // k-tiles per row
   int n_blocks;     // row blocks
+  int split;        // CTAs per row block (a cluster; 1: no split of K)
+  int kt_per_cta;   // k-tiles each CTA of a row block takes
   int stages;       // ring depth
   int stage_bytes;  // bytes of one stage (weights, then scales and biases)
   unsigned flags;
@@ -77,6 +80,7 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
   const int xs_m = xs_floats(sh.rounds, BITS);  // floats per row of x (transposed layout)
 
   // shared memory: [stages][stage_bytes] | x (f32) | xsum (f32x2) | scale pairs | barriers
+  //                | split-K receive buffer [split-1][warp][R*MT] (f32)
   uint8_t* ring = smem;
   float* xs = reinterpret_cast<float*>(ring + size_t(sh.stages) * sh.stage_bytes);
   float2* xsum = reinterpret_cast<float2*>(xs + MT * xs_m);
@@ -84,9 +88,18 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(sb32 + kConsumerWarps * R * 32);
   const uint32_t ring_u32 = ptx::smem_u32(ring);
   const uint32_t full0 = ptx::smem_u32(bars), empty0 = full0 + 8u * sh.stages;
+  float* red = reinterpret_cast<float*>(bars + 2 * sh.stages);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m0 = blockIdx.y * MT;
+  // split > 1: a cluster of `split` CTAs shares one row block, CTA c taking
+  // k-tiles [c, c+1) * kt_per_cta; otherwise the grid is persistent over the
+  // row blocks
+  const int split = sh.split;
+  const int crank = split > 1 ? int(ptx::cluster_ctarank()) : 0;
+  const int blk0 = split > 1 ? int(blockIdx.x) / split : int(blockIdx.x);
+  const int blk_step = split > 1 ? sh.n_blocks : int(gridDim.x);
+  const int kt_lo = crank * sh.kt_per_cta, kt_hi = kt_lo + sh.kt_per_cta;
 
   // the next kernel may launch at once: it only streams its own (read-only)
   // weights before its own dependency wait, which this kernel's completion
@@ -100,6 +113,9 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
     ptx::fence_mbar_init();
   }
   __syncthreads();
+  // (split-K) first half of the barrier that tells every CTA of the cluster
+  // that the others have started: their shared memory may then be written
+  if (split > 1) ptx::cluster_arrive_relaxed();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -110,10 +126,10 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
     bool ok = true;
     const uint32_t w_bytes = uint32_t(sh.kt_bytes);
     const uint32_t sb_bytes = kScaleCopy ? uint32_t(kt_groups * 2) : 0u;
-    for (int blk = blockIdx.x; blk < sh.n_blocks && ok; blk += gridDim.x) {
+    for (int blk = blk0; blk < sh.n_blocks && ok; blk += blk_step) {
       const int row0 = blk * kRB;
       const int nr = min(kRB, N - row0);
-      for (int kt = 0; kt < sh.n_kt; ++kt) {
+      for (int kt = kt_lo; kt < kt_hi; ++kt) {
         if (round > 0 && !ptx::mbar_wait(empty0 + 8u * s, (round - 1) & 1u)) {
           if (lane == 0) atomicOr(&g_qmv_status, 1u);
           ok = false;
@@ -166,6 +182,13 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
         if (!ptx::mbar_wait(full0 + 8u * (v % sh.stages), uint32_t(v / sh.stages) & 1u))
           if (lane == 0) atomicOr(&g_qmv_status, 16u);
     }
+    if (split > 1) {
+      // the producer takes part in the cluster barriers of the reduction
+      __syncwarp();
+      ptx::cluster_wait();
+      ptx::cluster_arrive_release();
+      ptx::cluster_wait();
+    }
     return;
   }
 
@@ -173,32 +196,40 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
   // x is produced by the preceding kernel: wait for it (a no-op unless this is
   // a programmatic dependent launch).
   grid_dependency_wait();
-  stage_x<BITS, MT, AT, false>(x + int64_t(m0) * K, K, sh.M - m0, K, sh.rounds, xs, xsum, tid);
+  // a split CTA stages only the part of x its k-tiles read
+  const int k_lo = kt_lo * sh.kt_bytes * (8 / BITS);
+  stage_x<BITS, MT, AT, false>(x + int64_t(m0) * K + k_lo, K, sh.M - m0,
+                               sh.kt_per_cta * sh.kt_bytes * (8 / BITS), sh.rounds, xs, xsum, tid);
 
   const StageGeom geom{sh.kt_bytes, kt_groups, sh.rounds, gpr, N};
   float2* sbw = sb32 + warp * R * 32;
   int s = 0;
   uint32_t round = 0;
-  for (int blk = blockIdx.x; blk < sh.n_blocks; blk += gridDim.x) {
+  for (int blk = blk0; blk < sh.n_blocks; blk += blk_step) {
     const int rb0 = blk * kRB + warp * R;  // this warp's first row
     float2 acc[R][MT];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
       for (int mm = 0; mm < MT; ++mm) acc[r][mm] = make_float2(0.0f, 0.0f);
-    for (int kt = 0; kt < sh.n_kt; ++kt) {
+    bool failed = false;
+    for (int kt = kt_lo; kt < kt_hi; ++kt) {
       if (!ptx::mbar_wait(full0 + 8u * s, round & 1u)) {
         if (lane == 0) atomicOr(&g_qmv_status, 2u);
-        return;  // no CTA-wide barrier follows: leaving is safe
+        // no CTA-wide barrier follows: leaving is safe, except that a split
+        // CTA still takes part in the cluster barriers below
+        if (split == 1) return;
+        failed = true;
+        break;
       }
       const uint8_t* stage = ring + size_t(s) * sh.stage_bytes;
       if constexpr (MODE == 2) {
         stage_scales_f32<BITS, R, AT>(stage, kRB, warp * R, sbw, lane);
-        accumulate_fixed<BITS, MT, R, AT>(stage, warp * R, kt, sbw, xs, xs_m, xsum,
+        accumulate_fixed<BITS, MT, R, AT>(stage, warp * R, kt - kt_lo, sbw, xs, xs_m, xsum,
                                           sh.rounds * 32, lane, acc);
       } else {
-        accumulate_stage<BITS, MT, R, AT>(stage, kRB, warp * R, kt, geom, kScaleCopy, scales,
-                                          biases, rb0, xs, xsum, lane, acc);
+        accumulate_stage<BITS, MT, R, AT>(stage, kRB, warp * R, kt, kt - kt_lo, geom, kScaleCopy,
+                                          scales, biases, rb0, xs, xsum, lane, acc);
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(empty0 + 8u * s);
@@ -207,11 +238,35 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
         ++round;
       }
     }
-    if constexpr (EPI)
-      store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, static_cast<void*>(y), N,
-                            static_cast<const AT*>(sh.ep.bias), sh.ep.y_f32 != 0);
-    else
-      store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, y, N);
+    const AT* lbias = EPI ? static_cast<const AT*>(sh.ep.bias) : nullptr;
+    const bool yf32 = EPI && sh.ep.y_f32 != 0;
+    if (split == 1) {
+      store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, static_cast<void*>(y), N, lbias, yf32);
+      continue;
+    }
+    // ------------------------------------------------ split-K reduction
+    // Every CTA reduces its partial sums across lanes; CTAs 1.. store theirs
+    // into CTA 0's receive buffer, and CTA 0 adds them in rank order to its
+    // own and stores the rows.  (With split > 1 this loop runs once.)
+    using RS = RowSums<MT, R>;
+    float total = RS::reduce(acc, lane);
+    const int vi = RS::value_index(lane);
+    ptx::cluster_wait();  // every CTA of the cluster has started
+    if (crank != 0 && RS::owner(lane) && !failed)
+      ptx::st_cluster_f32(
+          ptx::map_shared_rank(ptx::smem_u32(red + ((crank - 1) * kConsumerWarps + warp) * RS::kV +
+                                             vi),
+                               0u),
+          total);
+    ptx::cluster_arrive_release();
+    ptx::cluster_wait();  // the partials are in CTA 0's buffer
+    if (crank == 0) {
+      for (int src = 0; src < split - 1; ++src)
+        total += red[(src * kConsumerWarps + warp) * RS::kV + vi];
+      const int row = rb0 + vi / MT, m = m0 + vi % MT;
+      if (RS::owner(lane) && row < N && m < sh.M)
+        store_value<AT>(total, row, m, static_cast<void*>(y), N, lbias, yf32);
+    }
   }
 }
 
@@ -220,7 +275,7 @@ size_t smem_for(const Shape& sh, int MT, int R, int bits) {
   const int cw = 128 / bits;
   return size_t(sh.stages) * sh.stage_bytes + size_t(MT) * sh.rounds * 32 * cw * 4 +
          size_t(MT) * sh.rounds * 32 * 8 + size_t(kConsumerWarps) * R * 32 * 8 +
-         size_t(sh.stages) * 16;
+         size_t(sh.stages) * 16 + size_t(sh.split - 1) * kConsumerWarps * R * MT * 4;
 }
 
 template <int BITS, int MT, int R, typename AT, int MODE, bool EPI>
@@ -264,19 +319,32 @@ qlin_status launch_t(const void* x, const uint32_t* wq, const void* scales, cons
   if (m_tiles > 65535) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmv: M too large");
   const int64_t resident = int64_t(blocks_per_sm) * sm_count();
   const int64_t per_tile = std::max<int64_t>(1, resident / std::min<int64_t>(m_tiles, resident));
-  const int64_t gx = std::max<int64_t>(1, std::min<int64_t>(sh.n_blocks, per_tile));
+  // split K: exactly one cluster of `split` CTAs per row block (the kernel's
+  // reduction relies on it); otherwise persistent over the row blocks
+  const int64_t gx = sh.split > 1
+                         ? int64_t(sh.n_blocks) * sh.split
+                         : std::max<int64_t>(1, std::min<int64_t>(sh.n_blocks, per_tile));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(gx), unsigned(m_tiles), 1u);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned n_attr = 0;
   if (sh.flags & QLIN_OVERLAP_PREVIOUS) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
   }
+  if (sh.split > 1) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = unsigned(sh.split);
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
+  cfg.attrs = n_attr ? attr : nullptr;
+  cfg.numAttrs = n_attr;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<const AT*>(x), wq,
                                            static_cast<const AT*>(scales),
                                            static_cast<const AT*>(biases), static_cast<AT*>(y),
@@ -288,36 +356,71 @@ qlin_status launch_t(const void* x, const uint32_t* wq, const void* scales, cons
   return check_launch("qmv_kernel");
 }
 
+// Rows per consumer warp: two (x reuse, fewer blocks) when rows are
+// plentiful, one when the launch would otherwise leave SMs idle (four rows
+// per warp needs ~150 registers and halves the resident warps: slower).
+// QLIN_QMV_R (1 or 2) overrides it, for tuning.
+int rows_per_warp(int64_t N, int64_t sms) {
+  if (const char* env = std::getenv("QLIN_QMV_R")) {
+    const int v = std::atoi(env);
+    if (v == 1 || v == 2) return v;
+  }
+  return N >= 16 * 2 * sms ? 2 : 1;
+}
+
+// CTAs per row block.  K is split over a cluster only when the row blocks are
+// too few to occupy the SMs (two CTAs each) and long: a split costs about
+// 1 us (cluster launch and barriers) whatever its size, which a block of up
+// to 16 KB of packed weights does not win back (measured on 300 x 512,
+// 512 x 2048 and 1029 x 2048), while 129 rows of K = 8192 at 4 bits (32 KB a
+// block) fell from 6.0 to 4.1 us.  The factor is the largest of 8, 4, 2 whose
+// CTAs fit at once and leave each CTA at least 4 KB of the block.
+// QLIN_QMV_SPLIT (1, 2, 4 or 8) overrides the choice, for tuning, wherever
+// each CTA's share of a row is still a whole number of 16-byte chunks.
+constexpr int64_t kMinSplitBlockBytes = 32 * 1024;
+constexpr int64_t kMinSplitShareBytes = 4 * 1024;
+
+int qmv_split(int n_blocks, int row_bytes, int rows_per_block, int sms) {
+  auto divides = [&](int s) { return row_bytes % (16 * s) == 0; };
+  if (const char* env = std::getenv("QLIN_QMV_SPLIT")) {
+    const int v = std::atoi(env);
+    if (v == 1 || v == 2 || v == 4 || v == 8) return divides(v) ? v : 1;
+  }
+  const int64_t block_bytes = int64_t(rows_per_block) * row_bytes;
+  if (block_bytes < kMinSplitBlockBytes) return 1;
+  for (int s = 8; s >= 2; s /= 2)
+    if (int64_t(n_blocks) * s <= 2 * int64_t(sms) && divides(s) &&
+        block_bytes / s >= kMinSplitShareBytes)
+      return s;
+  return 1;
+}
+
 template <int BITS, int MT, typename AT>
 qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
                         const void* biases, void* y, Shape sh, cudaStream_t st) {
   const int64_t sms = sm_count();
   const int row_bytes = sh.K * BITS / 8;
   const int gpr = sh.K / kGroup;
-  // rows per consumer warp: two (x reuse, fewer blocks) when rows are
-  // plentiful, one when the launch would otherwise leave SMs idle (four rows
-  // per warp needs ~150 registers and halves the resident warps: slower)
-  int R = sh.N >= 16 * 2 * sms ? 2 : 1;
-  // QLIN_QMV_R (1 or 2) overrides the rows per warp, for tuning
-  if (const char* env = std::getenv("QLIN_QMV_R")) {
-    const int v = std::atoi(env);
-    if (v == 1 || v == 2) R = v;
-  }
+  const int R = rows_per_warp(sh.N, sms);
   const int RB = kConsumerWarps * R;
   const bool sb_aligned = (reinterpret_cast<uintptr_t>(scales) % 16) == 0 &&
                           (reinterpret_cast<uintptr_t>(biases) % 16) == 0;
+  const int n_blocks = (sh.N + RB - 1) / RB;
+  const int split = qmv_split(n_blocks, row_bytes, RB, int(sms));
+  sh.split = split;
   int mode;
-  if (sh.K % FixedTile<BITS>::kCodes == 0 && sb_aligned) {
+  if (sh.K % (FixedTile<BITS>::kCodes * split) == 0 && sb_aligned) {
     // fast path: 2048-code k-tiles, scales copied into the stage
     mode = 2;
     sh.kt_bytes = FixedTile<BITS>::kBytes;
     sh.n_kt = row_bytes / sh.kt_bytes;
   } else {
-    // k-tile: stages of about 32 KB of weights: the whole row when it fits,
-    // else the smallest split into equal 16-byte-multiple tiles that does
+    // k-tile: stages of about 32 KB of weights: the whole row (or the CTA's
+    // share of it) when it fits, else the smallest split into equal
+    // 16-byte-multiple tiles that does; a multiple of `split` tiles
     const int kt_max = std::max(512, 32768 / RB);
-    int n_kt = 1;
-    while (row_bytes / n_kt > kt_max || row_bytes % n_kt || (row_bytes / n_kt) % 16) ++n_kt;
+    int n_kt = split;
+    while (row_bytes / n_kt > kt_max || row_bytes % n_kt || (row_bytes / n_kt) % 16) n_kt += split;
     sh.n_kt = n_kt;
     sh.kt_bytes = row_bytes / n_kt;
     const int kt_codes = sh.kt_bytes * (8 / BITS);
@@ -330,7 +433,9 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
   const int kt_groups = sh.kt_bytes * (8 / BITS) / kGroup;
   sh.stage_bytes = RB * sh.kt_bytes + (mode != 0 ? 2 * RB * kt_groups * 2 : 0);
   sh.stage_bytes = (sh.stage_bytes + 127) / 128 * 128;
-  sh.n_blocks = (sh.N + RB - 1) / RB;
+  sh.n_blocks = n_blocks;
+  sh.kt_per_cta = sh.n_kt / split;
+  sh.rounds = (sh.C / split + 31) / 32;
   // ring depth: about 96 KB of stages, so that two CTAs fit on an SM
   // (QLIN_QMV_RING_KB overrides the target, for tuning)
   int ring_kb = 96;
@@ -391,6 +496,11 @@ qlin_status launch_qmv(const void* x, const uint32_t* wq, const void* scales, co
   return bits == 4 ? dispatch<4, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, ep, st)
                    : dispatch<8, __nv_bfloat16>(x, wq, scales, biases, y, M, N, K, flags, ep,
                                                 st);
+}
+
+int qmv_plan_split(int64_t N, int64_t K, int bits, int sms) {
+  const int RB = kConsumerWarps * rows_per_warp(N, sms);
+  return qmv_split(int((N + RB - 1) / RB), int(K * bits / 8), RB, sms);
 }
 
 cudaError_t qmv_take_device_status(unsigned* flags) {

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_chain_kernel(const __grid_con
           stage_scales_f32<BITS, kR, AT>(stage, kRB, warp * kR, sbw, lane);
           accumulate_fixed<BITS, 1, kR, AT>(stage, warp * kR, kt, sbw, xs, 0, xsum, 0, lane, acc);
         } else {
-          accumulate_stage<BITS, 1, kR, AT>(stage, kRB, warp * kR, kt, geom, L.scale_copy != 0,
+          accumulate_stage<BITS, 1, kR, AT>(stage, kRB, warp * kR, kt, kt, geom, L.scale_copy != 0,
                                             sc, bi, row0, xs, xsum, lane, acc);
         }
         __syncwarp();

@@ -174,10 +174,11 @@ struct StageGeom {
 };
 
 // Accumulate one stage into acc for the R rows (block rows w0 .. w0+R-1, global
-// rows row0 ..) this warp owns; k-tile kt of the row.
+// rows row0 ..) this warp owns; k-tile kt of the row, which is k-tile kt_x of
+// the staged x (kt_x = kt unless x was staged from a later k-tile on).
 template <int BITS, int MT, int R, typename AT>
 __device__ __forceinline__ void accumulate_stage(const uint8_t* stage, int RB, int w0, int kt,
-                                                 const StageGeom& g, bool scale_copy,
+                                                 int kt_x, const StageGeom& g, bool scale_copy,
                                                  const AT* __restrict__ scales,
                                                  const AT* __restrict__ biases, int row0,
                                                  const float* xs, const float2* xsum, int lane,
@@ -193,6 +194,7 @@ __device__ __forceinline__ void accumulate_stage(const uint8_t* stage, int RB, i
   const AT* bst = sst + RB * g.kt_groups;
   for (int cl = lane; cl < kt_chunks; cl += 32) {
     const int c = kt * kt_chunks + cl;   // chunk index within the row
+    const int cx = kt_x * kt_chunks + cl;  // chunk index within the staged x
     const int gl = (cl * kCW) / kGroup;  // group within the k-tile
     uint4 cw[R];
     float2 s2[R], b2[R];
@@ -212,7 +214,7 @@ __device__ __forceinline__ void accumulate_stage(const uint8_t* stage, int RB, i
       s2[r] = make_float2(sv, sv);
       b2[r] = make_float2(bv, bv);
     }
-    const float* xbase = xs + ((c >> 5) * (kCW / 4) * 32 + (c & 31)) * 4;
+    const float* xbase = xs + ((cx >> 5) * (kCW / 4) * 32 + (cx & 31)) * 4;
     float2 P[R][MT];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -243,7 +245,7 @@ __device__ __forceinline__ void accumulate_stage(const uint8_t* stage, int RB, i
     }
 #pragma unroll
     for (int mm = 0; mm < MT; ++mm) {
-      const float2 X = xsum[mm * g.rounds * 32 + c];
+      const float2 X = xsum[mm * g.rounds * 32 + cx];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const float2 D = __ffma2_rn(neg_magic, X, P[r][mm]);
@@ -284,6 +286,7 @@ __device__ __forceinline__ void stage_scales_f32(const uint8_t* stage, int RB, i
   __syncwarp();
 }
 
+// kt: the k-tile of the staged x (the packed tile is the stage itself).
 template <int BITS, int MT, int R, typename AT>
 __device__ __forceinline__ void accumulate_fixed(const uint8_t* stage, int w0, int kt,
                                                  const float2* sb32, const float* xs, int xs_m,
@@ -350,29 +353,50 @@ __device__ __forceinline__ void accumulate_fixed(const uint8_t* stage, int w0, i
   }
 }
 
+// The warp-wide sums of the R x MT accumulators.  Lane l ends with value
+// index vi = l / (32 / (R*MT)), i.e. row vi / MT and token vi % MT of the
+// warp's rows; the first lane of each such run is the one that stores it.
+template <int MT, int R>
+struct RowSums {
+  static constexpr int kV = R * MT;
+  static constexpr int kLanesPerValue = 32 / kV;
+  static __device__ __forceinline__ int value_index(int lane) { return lane / kLanesPerValue; }
+  static __device__ __forceinline__ bool owner(int lane) { return lane % kLanesPerValue == 0; }
+  static __device__ __forceinline__ float reduce(float2 (&acc)[R][MT], int lane) {
+    float v[kV];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int mm = 0; mm < MT; ++mm) v[r * MT + mm] = acc[r][mm].x + acc[r][mm].y;
+    return butterfly_sum<kV>(v, lane);
+  }
+};
+
+// Store one finished sum: a linear layer's bias joins the f32 sum before the
+// one rounding (or the f32 value is stored as it is).
+template <typename AT>
+__device__ __forceinline__ void store_value(float total, int row, int m, void* __restrict__ y,
+                                            int64_t ldy, const AT* __restrict__ layer_bias,
+                                            bool y_f32) {
+  if (layer_bias) total += Act<AT>::to_f32(layer_bias[row]);
+  if (y_f32)
+    static_cast<float*>(y)[int64_t(m) * ldy + row] = total;
+  else
+    static_cast<AT*>(y)[int64_t(m) * ldy + row] = Act<AT>::from_f32_rn(total);
+}
+
 // Reduce the warp's R x MT sums across lanes and store them (row-major y with
 // leading dimension ldy).  Returns true on the lanes that stored a value.
 template <int MT, int R, typename AT>
 __device__ __forceinline__ bool store_rows(float2 (&acc)[R][MT], int lane, int row0, int m0,
                                            int N, int M, void* __restrict__ y, int64_t ldy,
                                            const AT* __restrict__ layer_bias, bool y_f32) {
-  constexpr int kV = R * MT;
-  float v[kV];
-#pragma unroll
-  for (int r = 0; r < R; ++r)
-#pragma unroll
-    for (int mm = 0; mm < MT; ++mm) v[r * MT + mm] = acc[r][mm].x + acc[r][mm].y;
-  float total = butterfly_sum<kV>(v, lane);
-  constexpr int kLanesPerValue = 32 / kV;
-  const int vi = lane / kLanesPerValue;
+  using RS = RowSums<MT, R>;
+  const float total = RS::reduce(acc, lane);
+  const int vi = RS::value_index(lane);
   const int row = row0 + vi / MT, m = m0 + vi % MT;
-  if ((lane % kLanesPerValue) == 0 && row < N && m < M) {
-    // a linear layer's bias joins the f32 sum before the one rounding
-    if (layer_bias) total += Act<AT>::to_f32(layer_bias[row]);
-    if (y_f32)
-      static_cast<float*>(y)[int64_t(m) * ldy + row] = total;
-    else
-      static_cast<AT*>(y)[int64_t(m) * ldy + row] = Act<AT>::from_f32_rn(total);
+  if (RS::owner(lane) && row < N && m < M) {
+    store_value<AT>(total, row, m, y, ldy, layer_bias, y_f32);
     return true;
   }
   return false;

@@ -164,3 +164,30 @@ def test_crossover_by_dtype(L):
     assert L.qlin_crossover_m_dtype(2048, 8192, 4, q.QLIN_BF16) == 8
     assert L.qlin_crossover_m_dtype(8192, 2048, 8, q.QLIN_BF16) == 8
     assert L.qlin_crossover_m(2048, 8192, 4) == L.qlin_crossover_m_dtype(2048, 8192, 4, q.QLIN_F16)
+
+
+def test_qmv_split_choice(L, monkeypatch):
+    """qmv splits K over a cluster only for few, long row blocks (at least
+    32 KB of packed weights each), by the largest factor whose CTAs fit on the
+    SMs two at a time with at least 4 KB of the block each."""
+    monkeypatch.delenv("QLIN_QMV_SPLIT", raising=False)
+    monkeypatch.delenv("QLIN_QMV_R", raising=False)
+    f = L.qlin_testing_qmv_split
+    assert f(300, 512, 4, 152) == 1          # 2 KB blocks: a split does not pay
+    assert f(1029, 2048, 8, 152) == 1        # 16 KB blocks
+    assert f(129, 8192, 4, 152) == 8         # 17 blocks of 32 KB
+    assert f(37, 16384, 8, 152) == 8
+    assert f(513, 8192, 8, 152) == 4         # 65 blocks: 8 would not fit at once
+    assert f(1000, 4096, 8, 152) == 2        # 125 blocks
+    assert f(2048, 8192, 8, 152) == 1        # 256 blocks already fill the SMs
+    assert f(129, 8192, 4, 16) == 1          # 17 blocks on 16 SMs
+    assert f(129, 8192, 4, 40) == 4
+    # invalid arguments
+    assert f(0, 512, 4, 152) == -1
+    assert f(300, 100, 4, 152) == -1
+    assert f(300, 512, 3, 152) == -1
+    assert f(300, 512, 4, 0) == -1
+    # the tuning override, where each CTA's share stays whole 16-byte chunks
+    monkeypatch.setenv("QLIN_QMV_SPLIT", "4")
+    assert f(300, 512, 4, 152) == 4          # 256-byte rows: 64 bytes a CTA
+    assert f(3, 192, 4, 152) == 1            # 96-byte rows do not split in 4

@@ -175,6 +175,64 @@ def test_one_hot_rows_exact_under_split_k(dev, qmm_tile, bits, dt):
     assert torch.equal(y.cpu(), w_hat[:, cols].t().contiguous().cpu())
 
 
+@pytest.fixture
+def qmv_split(monkeypatch):
+    """Force qmv's split of K over a cluster of CTAs (QLIN_QMV_SPLIT)."""
+    def force(split):
+        monkeypatch.setenv("QLIN_QMV_SPLIT", str(split))
+    return force
+
+
+QMV_SPLIT_CASES = [
+    # (split, m, n, k, bits, dt); k-tile kinds: fixed 2048-code tiles (K a
+    # multiple of 2048 * split), tiles with their scales copied, scales read
+    # from global memory (small tiles)
+    (1, 1, 129, 8192, 4, "f16"), (2, 1, 640, 2048, 8, "f16"), (4, 3, 300, 4096, 4, "bf16"),
+    (8, 1, 129, 8192, 4, "f16"), (8, 1, 37, 16384, 8, "bf16"), (4, 2, 1000, 8192, 8, "bf16"),
+    (8, 2, 1000, 8192, 8, "bf16"), (4, 1, 300, 512, 4, "f16"), (8, 5, 77, 1024, 8, "f16"),
+]
+
+
+@pytest.mark.parametrize("split,m,n,k,bits,dt", QMV_SPLIT_CASES)
+def test_qmv_split_k_factors(dev, qmv_split, split, m, n, k, bits, dt):
+    """qmv with K split over a cluster (each CTA's row sums added in CTA 0's
+    shared memory, in rank order) stays within the oracle's tolerance, plain
+    and with a linear layer's bias and float32 output."""
+    w, x, ref = case(8100 + split * 31 + n, m, n, k, bits, dt)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    qmv_split(split)
+    buf, y = guarded((m, n), TORCH_DT[dt], dev)
+    q.qmv(x.to(dev), wq, sc, bi, bits, out=y)
+    torch.cuda.synchronize()
+    assert canaries_intact(buf)
+    assert_within_tolerance(y, ref, f"qmv split={split} m={m} n={n} k={k} b={bits} {dt}")
+    if m < q.crossover_m(n, k, bits, TORCH_DT[dt]):
+        rng = np.random.default_rng(8200 + n)
+        b = torch.from_numpy(rng.standard_normal(n).astype(np.float32) * 0.5).to(TORCH_DT[dt])
+        y_ref, a_ref = O.matmul_bias_ref(x.double().numpy(), ref["w_hat"], b.double().numpy())
+        yl = q.linear(x.to(dev), wq, sc, bi, bits, bias=b.to(dev), out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert_within_tolerance(yl, {"y_ref": y_ref, "a_ref": a_ref}, f"linear split={split}")
+    assert q.device_status() == 0
+
+
+@pytest.mark.parametrize("bits,dt", [(4, "f16"), (8, "bf16")])
+def test_qmv_one_hot_rows_exact_under_split_k(dev, qmv_split, bits, dt):
+    """With x = e_k one CTA of each cluster holds the only nonzero term and
+    the others add exact zeros: qmv still reproduces the materialised
+    reconstruction bit for bit."""
+    n, k = 260, 512
+    w = S.weights_f32(79, n, k)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    cols = np.array([0, 1, 7, 63, 64, 200, 255, 256, 511])
+    x = torch.zeros((cols.size, k), dtype=TORCH_DT[dt])
+    x[np.arange(cols.size), cols] = 1
+    qmv_split(4)
+    y = q.qmv(x.to(dev), wq, sc, bi, bits)
+    w_hat = q.dequant(wq, sc, bi, bits)
+    assert torch.equal(y.cpu(), w_hat[:, cols].t().contiguous().cpu())
+
+
 @pytest.mark.parametrize("fn", ["qmv", "qmm"])
 @pytest.mark.parametrize("bits,dt", [(4, "f16"), (8, "f16"), (4, "bf16"), (8, "bf16")])
 def test_one_hot_rows_reproduce_dequant_bit_exactly(dev, fn, bits, dt):
