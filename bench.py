@@ -385,14 +385,54 @@ def flush_l2(buf):
     buf[: buf.numel() // 2].sum()
 
 
-def time_qmm(q, device, peaks, reps: int = 100, warm: int = 10):
-    """Tensor-core qmm on the prefill shapes (M = 512 and 2048), L2 flushed
-    between timed launches."""
+def l2_bytes(device) -> int:
+    import torch
+    return int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 0)) or 132 << 20
+
+
+def rotation_sets(bytes_per_set: int, device) -> int:
+    """Distinct input sets whose total is 2.5x the L2 size (at least 3)."""
+    return max(3, -(-int(2.5 * l2_bytes(device)) // max(1, bytes_per_set)))
+
+
+def time_rotating(launch, sets: int, device, reps: int = 5) -> float:
+    """Mean GPU seconds per launch of launch(i), i = 0 .. sets-1, each on its
+    own inputs and outputs (together larger than L2, so no launch finds its
+    operands there), run back to back in one CUDA graph replayed `reps`
+    times between two CUDA events on the launching stream."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(sets):
+            launch(i)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    del g
+    return e0.elapsed_time(e1) * 1e-3 / (reps * sets)
+
+
+def _replicas(t, sets):
+    return [t] + [t.clone() for _ in range(sets - 1)]
+
+
+def time_qmm(q, device, peaks):
+    """Tensor-core qmm on the prefill shapes (M = 512 and 2048): launches back
+    to back over rotating copies of the operands (2.5x the L2 size in all),
+    in one CUDA graph; and, as a diagnostic, the median of single launches
+    with L2 flushed before each."""
     import torch
 
     from int8_qmv_qmm_gb300 import synthetic as S
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
     rows = []
     cases = [(m, b, nk) for m in (2048, 512) for b in (4, 8)
              for nk in ((8192, 2048), (2048, 8192), (2048, 2048))]
@@ -402,45 +442,45 @@ def time_qmm(q, device, peaks, reps: int = 100, warm: int = 10):
         del w
         x = S.activations(4, m, k, "f16", outlier_frac=0.01).to(device)
         y = torch.empty((m, n), dtype=torch.float16, device=device)
-        for _ in range(warm):
-            q.qmm(x, wq, sc, bi, bits, out=y)
-        times = []
-        for _ in range(reps):
-            flush_l2(flush)
-            torch.cuda._sleep(100000)  # the host enqueues the events and launch meanwhile
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            q.qmm(x, wq, sc, bi, bits, out=y)
-            e1.record(stream)
-            e1.synchronize()
-            times.append(e0.elapsed_time(e1) * 1e-3)
-        t = statistics.median(times)
+        per_set = (x.numel() + y.numel() + 2 * sc.numel()) * 2 + wq.numel() * 4
+        sets = rotation_sets(per_set, device)
+        xs, wqs, scs, bis, ys = (_replicas(t, sets) for t in (x, wq, sc, bi, y))
+        t = time_rotating(lambda i: q.qmm(xs[i], wqs[i], scs[i], bis[i], bits, out=ys[i]),
+                          sets, device)
+        del xs, wqs, scs, bis, ys
+        t_iso = time_flushed(lambda: q.qmm(x, wq, sc, bi, bits, out=y), device, flush, reps=30)
         flops = 2.0 * m * n * k
         rows.append({"m": m, "n": n, "k": k, "bits": bits, "us": t * 1e6,
-                     "tflops": flops / t / 1e12})
+                     "tflops": flops / t / 1e12, "rotating_sets": sets,
+                     "isolated_flushed_us": t_iso * 1e6})
+    del flush
+    torch.cuda.empty_cache()
     best = max(r["tflops"] for r in rows)
     mean = statistics.mean(r["tflops"] for r in rows)
+    worst = min(r["tflops"] for r in rows)
     return {
-        "tflops_mean": mean, "tflops_best": best, "cases": rows,
+        "tflops_mean": mean, "tflops_best": best, "tflops_worst": worst, "cases": rows,
+        "timing": "us = GPU time per launch, launches back to back over rotating operand "
+                  "copies (2.5x L2) in one CUDA graph; isolated_flushed_us = median of single "
+                  "launches after an L2 flush (event overhead included)",
         "roofline": {"bound": "tensor", "achieved": mean, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": mean / peaks["bf16_tflops"],
+                     "frac_worst": worst / peaks["bf16_tflops"],
                      "traffic": None,
                      "note": f"f16 MMA; peak = dense bf16 burst ({peaks['source']}), "
                              "f16/bf16 nominal ratio 1"},
     }
 
 
-def crossover_sweep(q, device, reps: int = 100, warm: int = 10):
+def crossover_sweep(q, device):
     """qmv vs qmm on the batched-decode sweep (M = 1..32, 4-bit, bf16 as the
-    workload has it, and f16), L2 flushed between timed launches; per dtype the
-    crossover is the smallest M from which qmm is at least as fast on every
-    shape, next to the library's choice."""
+    workload has it, and f16), each timed back to back over rotating operand
+    copies (2.5x the L2 size); per dtype the crossover is the smallest M from
+    which qmm is at least as fast on every shape, next to the library's
+    choice."""
     import torch
 
     from int8_qmv_qmm_gb300 import synthetic as S
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
     out = {}
     for dt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
         table = []
@@ -448,35 +488,28 @@ def crossover_sweep(q, device, reps: int = 100, warm: int = 10):
             w = torch.from_numpy(S.weights_f32(S.weight_seed(3, n), n, k)).to(device)
             wq, sc, bi = q.quantize_affine(w, 4, sdtype=tdt)
             del w
+            sets = rotation_sets(wq.numel() * 4 + 2 * sc.numel() * 2, device)
+            wqs, scs, bis = (_replicas(t, sets) for t in (wq, sc, bi))
             for m in (1, 2, 4, 8, 16, 32):
                 x = S.activations(3, m, k, dt).to(device)
                 y = torch.empty((m, n), dtype=tdt, device=device)
                 row = {"n": n, "k": k, "m": m}
                 for name in ("qmv", "qmm"):
                     fn = getattr(q, name)
-                    for _ in range(warm):
-                        fn(x, wq, sc, bi, 4, out=y)
-                    ts = []
-                    for _ in range(reps):
-                        flush_l2(flush)
-                        torch.cuda._sleep(100000)  # the host enqueues the events and launch meanwhile
-                        e0 = torch.cuda.Event(enable_timing=True)
-                        e1 = torch.cuda.Event(enable_timing=True)
-                        e0.record(stream)
-                        fn(x, wq, sc, bi, 4, out=y)
-                        e1.record(stream)
-                        e1.synchronize()
-                        ts.append(e0.elapsed_time(e1) * 1e3)
-                    row[name + "_us"] = statistics.median(ts)
+                    t = time_rotating(lambda i: fn(x, wqs[i], scs[i], bis[i], 4, out=y), sets,
+                                      device)
+                    row[name + "_us"] = t * 1e6
                 row["packed_gbs_qmv"] = (wq.numel() * 4 + 2 * sc.numel() * 2) / row["qmv_us"] / 1e3
                 row["library_picks"] = "qmm" if m >= q.crossover_m(n, k, 4, tdt) else "qmv"
                 table.append(row)
+            del wqs, scs, bis
         cross = None
         for m in (1, 2, 4, 8, 16, 32):
             if all(r["qmm_us"] <= r["qmv_us"] for r in table if r["m"] == m):
                 cross = m
                 break
-        out[dt] = {"crossover_m": cross, "table": table}
+        out[dt] = {"crossover_m": cross, "table": table,
+                   "timing": "back to back over rotating weight copies (2.5x L2), one graph"}
     return out
 
 
@@ -503,44 +536,75 @@ def time_flushed(fn, device, flush, reps: int = 100, warm: int = 10):
 
 
 def small_workloads(q, device, peaks):
-    """The two M = 1 workloads below the L2 size, L2 flushed between timed
-    repetitions: the single 300 x 512 qmv (4-bit) and one Llama-3.2-1B
-    decoder layer's seven linears (4-bit), the latter both as the decode
-    step runs them (q/k/v and gate/up fused, 4 overlapped launches in one CUDA
-    graph) and as seven separate launches."""
+    """The two M = 1 workloads below the L2 size, each timed over rotating
+    copies of its weights (2.5x the L2 size, back to back in one CUDA graph)
+    and, as a diagnostic, as single launches after an L2 flush (median; event
+    overhead included): the single 300 x 512 qmv (4-bit) and one
+    Llama-3.2-1B decoder layer's seven linears (4-bit).  The layer is timed as
+    the decode step runs it (q/k/v and gate/up fused, 4 overlapped launches;
+    rotating = 8 distinct layers chained in one graph, time per layer) and as
+    seven separate launches."""
     import torch
 
     from int8_qmv_qmm_gb300 import synthetic as S
     from int8_qmv_qmm_gb300.decode_step import DecodeStep
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
-    out = {}
+    hbm = peaks["hbm_gbs"]
+
+    def rec(t, t_iso, b, **extra):
+        return dict(extra, us=t * 1e6, algorithmic_bytes=b, gbs=b / t / 1e9,
+                    frac=b / t / 1e9 / hbm, isolated_flushed_us=t_iso * 1e6)
+
+    out = {"timing": "us: back to back over rotating weight copies (2.5x L2) in one CUDA "
+                     "graph; isolated_flushed_us: median single launch after an L2 flush"}
     # single qmv: M = 1, K = 512, N = 300 (N not a multiple of 4)
     w = torch.from_numpy(S.weights_f32(0, 300, 512)).to(device)
     wq, sc, bi = q.quantize_affine(w, 4, sdtype=torch.float16)
     x = S.activations(0, 1, 512, "f16").to(device)
     y = torch.empty((1, 300), dtype=torch.float16, device=device)
-    t = time_flushed(lambda: q.qmv(x, wq, sc, bi, 4, out=y), device, flush)
     b = wq.numel() * 4 + 2 * sc.numel() * 2 + (512 + 300) * 2
-    out["single_qmv_300x512_4bit"] = {"us": t * 1e6, "algorithmic_bytes": b,
-                                      "gbs": b / t / 1e9, "frac": b / t / 1e9 / peaks["hbm_gbs"]}
-    # one decoder layer, 4-bit, as the decode step runs it
+    sets = rotation_sets(b, device)
+    wqs, scs, bis = (_replicas(t, sets) for t in (wq, sc, bi))
+    t = time_rotating(lambda i: q.qmv(x, wqs[i], scs[i], bis[i], 4, out=y), sets, device)
+    del wqs, scs, bis
+    t_iso = time_flushed(lambda: q.qmv(x, wq, sc, bi, 4, out=y), device, flush)
+    out["single_qmv_300x512_4bit"] = rec(t, t_iso, b, rotating_sets=sets)
+    # one decoder layer, 4-bit, as the decode step runs it: 8 distinct layers
+    # chained (rotating), and one layer alone (flushed)
+    chained = DecodeStep(device, bits=4, dtype=torch.float16, seed=1, layers=8, lm_head=False)
+    chained.x0.copy_(S.activations(1, 1, 2048, "f16").to(device))
+    chained.capture()
+    for _ in range(2):
+        chained.replay()
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(20):
+        chained.replay()
+    e1.record()
+    torch.cuda.synchronize(device)
+    t8 = e0.elapsed_time(e1) * 1e-3 / 20 / 8
+    b = sum(chained.algorithmic_bytes()) / 8
+    del chained
     layer = DecodeStep(device, bits=4, dtype=torch.float16, seed=1, layers=1, lm_head=False)
     layer.x0.copy_(S.activations(1, 1, 2048, "f16").to(device))
     layer.capture()
-    t = time_flushed(layer.replay, device, flush)
-    b = sum(layer.algorithmic_bytes())
-    res = {"fused_4_launches_graph": {"us": t * 1e6, "algorithmic_bytes": b, "gbs": b / t / 1e9,
-                                      "frac": b / t / 1e9 / peaks["hbm_gbs"]}}
+    t_iso = time_flushed(layer.replay, device, flush)
+    res = {"fused_4_launches_graph": rec(t8, t_iso, b, rotating="8 distinct layers chained")}
     per = {}
     for i, (name, n, k) in enumerate(S.LLAMA_1B_LINEARS):
         _, _, _, _, lwq, lsc, lbi, wseed = layer.linear_rows(i)
         lwq, lsc, lbi = lwq.contiguous(), lsc.contiguous(), lbi.contiguous()
         xx = S.activations(wseed, 1, k, "f16").to(device)
         yy = torch.empty((1, n), dtype=torch.float16, device=device)
-        t = time_flushed(lambda: q.qmv(xx, lwq, lsc, lbi, 4, out=yy), device, flush)
         b = lwq.numel() * 4 + 2 * lsc.numel() * 2 + (k + n) * 2
-        per[name] = {"n": n, "k": k, "us": t * 1e6, "gbs": b / t / 1e9,
-                     "frac": b / t / 1e9 / peaks["hbm_gbs"]}
+        sets = rotation_sets(b, device)
+        wqs, scs, bis = (_replicas(tt, sets) for tt in (lwq, lsc, lbi))
+        t = time_rotating(lambda j: q.qmv(xx, wqs[j], scs[j], bis[j], 4, out=yy), sets, device)
+        del wqs, scs, bis
+        t_iso = time_flushed(lambda: q.qmv(xx, lwq, lsc, lbi, 4, out=yy), device, flush)
+        per[name] = rec(t, t_iso, b, n=n, k=k, rotating_sets=sets)
     res["separate_launches"] = per
     out["decoder_layer_4bit"] = res
     del layer, flush
@@ -869,6 +933,8 @@ def profile_case(which: str, launches: int = 3):
     kernel on one workload shape (no timing, no oracle).
       qmv: the lm_head of the decode step (M=1, 128256x2048, 8-bit, f16),
            279 MB of packed weights (above the L2 size);
+      qmv_qkv / qmv_o / qmv_gate_up / qmv_down: the step's other launch shapes
+           (ncu flushes L2 before each captured launch);
       qmm: M=2048, N=8192, K=2048, 4-bit, f16 (the largest prefill case);
       qmm_split: M=512, N=2048, K=8192, 4-bit (K split over 4-CTA clusters)."""
     import torch
@@ -878,7 +944,8 @@ def profile_case(which: str, launches: int = 3):
     from int8_qmv_qmm_gb300 import synthetic as S
     build_lib.build()
     dev = torch.device("cuda", 0)
-    cases = {"qmv": (1, 128256, 2048, 8, q.qmv), "qmv_o": (1, 2048, 2048, 8, q.qmv),
+    cases = {"qmv": (1, 128256, 2048, 8, q.qmv), "qmv_qkv": (1, 3072, 2048, 8, q.qmv),
+             "qmv_o": (1, 2048, 2048, 8, q.qmv),
              "qmv_gate_up": (1, 16384, 2048, 8, q.qmv), "qmv_down": (1, 2048, 8192, 8, q.qmv),
              "qmm": (2048, 8192, 2048, 4, q.qmm), "qmm8": (2048, 8192, 2048, 8, q.qmm),
              "qmm_sq": (2048, 2048, 2048, 8, q.qmm),
@@ -907,7 +974,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-qmm", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["qmv", "qmv_o", "qmv_gate_up", "qmv_down", "qmm",
+    ap.add_argument("--profile", choices=["qmv", "qmv_qkv", "qmv_o", "qmv_gate_up", "qmv_down", "qmm",
                                           "qmm8", "qmm_sq", "qmm_split"],
                     help="run a small fixed case for ncu instead of the benchmark")
     args = ap.parse_args()
