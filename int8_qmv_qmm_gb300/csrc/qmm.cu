@@ -954,10 +954,10 @@ qlin_status dispatch(const void* x, const uint32_t* wq, const void* scales, cons
                      unsigned flags, cudaStream_t st) {
   // Token tile and split-K factor: the pair with the smallest estimated time,
   // waves of tiles x stages per CTA x time per stage, + the reduction when K
-  // is split.  Measured on GB300, a stage takes about 0.43 us whatever BN:
-  // a 128 x N x 16 MMA takes about the same time for every N up to 256, and
-  // the stage's tcgen05.commit adds a fixed cost.  So wider tiles are free and
-  // narrower ones only pay when they remove a wave.  K is split over a
+  // is split.  Measured on GB300 for every tile from 32 to 256 tokens, a
+  // 64-k stage takes about 0.43 us whatever BN (the MMAs of a 256-token stage
+  // alone take 0.26 us; the stage's trip through the ring sets the rate).  So
+  // wider tiles are free and narrower ones only pay when they remove a wave.  K is split over a
   // cluster of 2 or 4 CTAs only when the split tiles fit on the SMs at once
   // and leave each CTA at least 4 stages; the reduction costs about 2.5 us +
   // 0.045 us per accumulator column a CTA sends.  Ties go to the larger tile.
