@@ -472,9 +472,15 @@ def time_qmm(q, device, peaks):
     }
 
 
+# the batched-decode sweep's token counts: the workload's 1, 2, 4, 8, 16, 32 and
+# the counts around qmv's 4-token tiles
+SWEEP_M = (1, 2, 3, 4, 5, 6, 8, 12, 16, 32)
+
+
 def crossover_sweep(q, device):
     """qmv vs qmm on the batched-decode sweep (M = 1..32, 4-bit, bf16 as the
-    workload has it, and f16), each timed back to back over rotating operand
+    workload has it, and f16; also M = 3, 5, 6, 12 around qmv's 4-token
+    tiles), each timed back to back over rotating operand
     copies (2.5x the L2 size); per dtype the crossover is the smallest M from
     which qmm is at least as fast on every shape, next to the library's
     choice."""
@@ -490,7 +496,7 @@ def crossover_sweep(q, device):
             del w
             sets = rotation_sets(wq.numel() * 4 + 2 * sc.numel() * 2, device)
             wqs, scs, bis = (_replicas(t, sets) for t in (wq, sc, bi))
-            for m in (1, 2, 4, 8, 16, 32):
+            for m in SWEEP_M:
                 x = S.activations(3, m, k, dt).to(device)
                 y = torch.empty((m, n), dtype=tdt, device=device)
                 row = {"n": n, "k": k, "m": m}
@@ -504,7 +510,7 @@ def crossover_sweep(q, device):
                 table.append(row)
             del wqs, scs, bis
         cross = None
-        for m in (1, 2, 4, 8, 16, 32):
+        for m in SWEEP_M:
             if all(r["qmm_us"] <= r["qmv_us"] for r in table if r["m"] == m):
                 cross = m
                 break

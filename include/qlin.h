@@ -263,10 +263,11 @@ qlin_status qlin_linear(const void* x, const uint32_t* wq, const void* scales,
                         int group_size, qlin_dtype dtype, void* stream);
 
 /* Smallest M for which qlin_linear picks the tensor-core path for activation
- * dtype `dtype`, from measurements on GB300 (8 for bf16; for f16 8 when
- * N >= K, 4 when K > N); the environment variable QLIN_CROSSOVER_M (read once
- * per process) overrides it.  No counterpart on the pages: an addition of
- * this library. */
+ * dtype `dtype`, from measurements on GB300: 4 for f16 when K > N; else 5
+ * when N*K >= 6*2^20 and 9 below (qmv reads the weights once per 4 tokens).
+ * `bits` does not change it (4- and 8-bit measured alike).  The environment
+ * variable QLIN_CROSSOVER_M (read once per process) overrides it.  No
+ * counterpart on the pages: an addition of this library. */
 int64_t qlin_crossover_m_dtype(int64_t N, int64_t K, int bits, qlin_dtype dtype);
 
 /* qlin_crossover_m_dtype for f16 activations. */

@@ -296,14 +296,17 @@ int64_t qlin_crossover_m_dtype(int64_t N, int64_t K, int bits, qlin_dtype dtype)
     return v >= 1 ? v : 0;
   }();
   if (env_m) return env_m;
-  // Measured on GB300 (batched-decode sweep, L2 flushed, 4- and 8-bit alike):
-  // with f16 the tensor-core kernel overtakes the CUDA-core one at M = 8 when
-  // N >= K (8192 x 2048: 16.4 vs 20.5 us) and at M = 4 when K > N (2048 x 8192:
-  // 22.5 vs 22.5 us); bf16 issues two MMAs per K step (the residual operand)
-  // and overtakes at M = 8 on both shapes (2048 x 8192 at M = 4: 28.7 vs
-  // 24.6 us, at M = 8: 28.7 vs 34.8 us).
-  if (dtype == QLIN_BF16) return 8;
-  return K > N ? 4 : 8;
+  // Measured on GB300 (batched decode, M = 2..16, weights rotated over 2.5x
+  // the L2 size; 4- and 8-bit alike, f16 and bf16).  qmv streams the weights
+  // once per tile of 4 tokens, so its time steps up at M = 5, 9, ...; qmm's
+  // stays flat for M <= 256.  On the larger matrices (N*K >= 6.3 M: 3072 x
+  // 2048, 8192 x 2048, 2048 x 8192) qmm is the faster from M = 5 (8192 x 2048,
+  // 8-bit f16, M = 6: 12.3 vs 16.1 us), and with f16 already at M = 4 when
+  // K > N (2048 x 8192: 17.7 vs 18.2 us).  On 2048 x 2048, where qmm has only
+  // 16 row tiles to spread, qmv stays the faster up to M = 8 (bf16, M = 8: 9.2
+  // vs 11.3 us; M = 12: 11.9 vs 11.3 us).
+  if (dtype == QLIN_F16 && K > N) return 4;
+  return N * K >= int64_t(6) * 1024 * 1024 ? 5 : 9;
 }
 
 int64_t qlin_crossover_m(int64_t N, int64_t K, int bits) {

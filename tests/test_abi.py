@@ -158,12 +158,20 @@ def test_testing_chain_entry_validation(L):
     assert call(0, 3000000) == INVALID
 
 
-def test_crossover_by_dtype(L):
-    """bf16 issues two MMAs per K step, so it switches to the tensor cores later."""
-    assert L.qlin_crossover_m_dtype(2048, 8192, 4, q.QLIN_F16) == 4
-    assert L.qlin_crossover_m_dtype(2048, 8192, 4, q.QLIN_BF16) == 8
-    assert L.qlin_crossover_m_dtype(8192, 2048, 8, q.QLIN_BF16) == 8
-    assert L.qlin_crossover_m(2048, 8192, 4) == L.qlin_crossover_m_dtype(2048, 8192, 4, q.QLIN_F16)
+def test_crossover_by_shape_and_dtype(L):
+    """The measured switch: qmm from M = 5 on the larger matrices (from M = 4
+    for f16 with K > N), from M = 9 on small ones, whatever the bit width."""
+    f16, bf16 = q.QLIN_F16, q.QLIN_BF16
+    for bits in (4, 8):
+        assert L.qlin_crossover_m_dtype(2048, 8192, bits, f16) == 4
+        assert L.qlin_crossover_m_dtype(2048, 8192, bits, bf16) == 5
+        assert L.qlin_crossover_m_dtype(8192, 2048, bits, bf16) == 5
+        assert L.qlin_crossover_m_dtype(8192, 2048, bits, f16) == 5
+        assert L.qlin_crossover_m_dtype(3072, 2048, bits, f16) == 5
+        assert L.qlin_crossover_m_dtype(2048, 2048, bits, f16) == 9
+        assert L.qlin_crossover_m_dtype(2048, 2048, bits, bf16) == 9
+        assert L.qlin_crossover_m_dtype(300, 512, bits, bf16) == 9
+    assert L.qlin_crossover_m(2048, 8192, 4) == L.qlin_crossover_m_dtype(2048, 8192, 4, f16)
 
 
 def test_qmv_split_choice(L, monkeypatch):

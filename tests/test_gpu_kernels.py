@@ -252,8 +252,9 @@ def test_one_hot_rows_reproduce_dequant_bit_exactly(dev, fn, bits, dt):
 
 def test_linear_dispatches_both_paths(dev):
     n, k, bits, dt = 300, 512, 4, "f16"
-    assert q.crossover_m(8192, 2048, 4) == 8 and q.crossover_m(2048, 8192, 4) == 4
-    assert q.crossover_m(2048, 8192, 8, torch.bfloat16) == 8
+    assert q.crossover_m(8192, 2048, 4) == 5 and q.crossover_m(2048, 8192, 4) == 4
+    assert q.crossover_m(2048, 8192, 8, torch.bfloat16) == 5
+    assert q.crossover_m(n, k, bits) == 9
     for m in (1, 40):
         w, x, ref = case(5 + m, m, n, k, bits, dt)
         wq, sc, bi = _upload(dev, w, bits, dt)
