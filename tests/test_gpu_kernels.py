@@ -254,7 +254,8 @@ def test_linear_dispatches_both_paths(dev):
     n, k, bits, dt = 300, 512, 4, "f16"
     assert q.crossover_m(8192, 2048, 4) == 5 and q.crossover_m(2048, 8192, 4) == 4
     assert q.crossover_m(2048, 8192, 8, torch.bfloat16) == 5
-    assert q.crossover_m(n, k, bits) == 9
+    assert q.crossover_m(n, k, bits) == 4                      # f16, K > N
+    assert q.crossover_m(n, k, bits, torch.bfloat16) == 9      # small matrix
     for m in (1, 40):
         w, x, ref = case(5 + m, m, n, k, bits, dt)
         wq, sc, bi = _upload(dev, w, bits, dt)
