@@ -496,9 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t fmt = std::is_same<AT, __half>::value ? 0u : 1u;
       constexpr uint32_t idesc = ptx::idesc_f16(fmt, kBM, BN);
-      int s = 0, g = 0, i = 0;
+      int s = 0, i = 0;
       uint32_t round = 0;
-      uint32_t full_ph = 0;  // bit g*8+s: parity of the next phase of full_bar(g, s)
       bool ok = true, any = false;
       for (int t = t_first; t < total_tiles && ok; t += t_step, ++i) {
         const int buf = i % L::kDBufs;
@@ -511,8 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(buf * BN);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!ptx::mbar_wait(afull_bar(s), round & 1u) ||
-              !ptx::mbar_wait(full_bar(g, s), (full_ph >> (g * 8 + s)) & 1u)) {
+          // A ready implies the stage's TMA bytes (x included) have landed:
+          // the dequantising warps arrive on afull only after they have
+          // waited for the stage's full barrier.  One wait per stage: this
+          // thread's own latency is part of the stage time.
+          if (!ptx::mbar_wait(afull_bar(s), round & 1u)) {
             report(kStatusMma);
             ok = false;
             break;
@@ -532,8 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           any = true;
           ptx::mma_commit(empty_bar(s));
-          full_ph ^= 1u << (g * 8 + s);
-          if (++g == kDequantGroups) g = 0;
           if (++s == stages) {
             s = 0;
             ++round;
