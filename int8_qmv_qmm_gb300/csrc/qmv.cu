@@ -25,6 +25,12 @@
 // reduction are in qmv_core.cuh.  Warp w computes rows w*R .. w*R+R-1 of each
 // stage; lanes take consecutive 16-byte chunks.  No global workspace.
 //
+// Split of K.  When the row blocks are few and long (small N, long K), a
+// thread-block cluster of 2, 4 or 8 CTAs shares each row block: CTA c takes
+// an equal share of the row's k-tiles and stages only the part of x they
+// read, and CTAs 1.. add their row sums into CTA 0's shared memory, which
+// stores the rows (the "split-K where N is small" of the M = 1 path).
+//
 // Every mbarrier wait is bounded; a wait that gives up sets a device status
 // bit and the CTA unwinds after its outstanding copies have landed.
 

@@ -216,6 +216,30 @@ def test_qmv_split_k_factors(dev, qmv_split, split, m, n, k, bits, dt):
     assert q.device_status() == 0
 
 
+def test_qmv_split_k_as_dependent_launch(dev):
+    """A split-K qmv (a cluster per row block) launched as a programmatic
+    dependent launch after the kernel that writes its input gives what a plain
+    launch gives, bit for bit (the cluster and the overlap attributes
+    together)."""
+    n, k, bits, dt = 129, 8192, 4, "f16"
+    assert q.lib().qlin_testing_qmv_split(n, k, bits, torch.cuda.get_device_properties(dev)
+                                          .multi_processor_count) > 1
+    w, x, ref = case(8300, 1, n, k, bits, dt)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    xd = x.to(dev)
+    plain = q.qmv(xd, wq, sc, bi, bits)
+    x2 = torch.empty_like(xd)
+    outs = []
+    for _ in range(3):
+        x2.copy_(xd)                       # the preceding kernel writes the input
+        outs.append(q.qmv(x2, wq, sc, bi, bits, overlap_previous=True))
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    assert_within_tolerance(plain, ref, "split qmv plain")
+    for o in outs:
+        assert torch.equal(o, plain)
+
+
 @pytest.mark.parametrize("bits,dt", [(4, "f16"), (8, "bf16")])
 def test_qmv_one_hot_rows_exact_under_split_k(dev, qmv_split, bits, dt):
     """With x = e_k one CTA of each cluster holds the only nonzero term and
