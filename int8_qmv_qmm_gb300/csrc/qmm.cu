@@ -671,20 +671,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // row-minor so that a warp's 16-byte stores fall in distinct banks.
     // Each owner then adds the partials in a fixed order (its own first,
     // then the sources by rank) and stores its slice.
-    const bool epi = warp >= 2 + kDequantWarps && t_first < total_tiles;
+    // Eight warps share the work: the four epilogue warps and the first
+    // dequantising warpgroup (idle by now), one of each per TMEM lane quarter.
+    // Part p of a quarter takes columns [p * half, p * half + half) of every
+    // slice (one part when a slice has fewer than 32 columns).
     const int slice = BN / split;
+    const int parts = slice >= 32 ? 2 : 1;
+    const int half = slice / parts;
+    const bool tile = t_first < total_tiles;
+    const bool epi_warp = warp >= 2 + kDequantWarps;
+    const bool helper_warp = warp >= 2 && warp < 2 + 4;  // dequant warpgroup 0
+    const int part = epi_warp ? 0 : 1;
+    const bool red = tile && (epi_warp || (helper_warp && parts == 2));
+    const int col0 = part * half;
     // arm the receive barrier with every byte the other CTAs will send
     // before any of them can start (the cluster barrier below)
-    if (threadIdx.x == 0 && t_first < total_tiles)
+    if (threadIdx.x == 0 && tile)
       ptx::mbar_arrive_expect_tx(red_bar, uint32_t((split - 1) * slice * kBM * 4));
     ptx::cluster_sync();  // every CTA of the cluster is past its K loop and armed
+    // (the accumulator is complete: the epilogue warps saw its commit before
+    // the CTA barrier; TMEM loads follow the thread synchronisation)
+    ptx::tc_fence_after();
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (uint32_t(quarter * 32) << 16);
     // batches of up to 64 columns: four TMEM loads, one wait
     constexpr int kRBatch = BN < 64 ? BN : 64;
-    const int batch = slice < kRBatch ? slice : kRBatch;
-    if (epi) {
+    const int batch = half < kRBatch ? half : kRBatch;
+    if (red) {
       for (int d = 0; d < split; ++d) {
         if (d == rank) continue;
         const int slot = rank < d ? rank : rank - 1;
@@ -692,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::map_shared_rank(base, uint32_t(d)) + uint32_t(slot * (slice / 4) * kBM * 16);
         const uint32_t dst_bar = ptx::map_shared_rank(red_bar, uint32_t(d));
 #pragma unroll 1
-        for (int c0 = 0; c0 < slice; c0 += batch) {
+        for (int c0 = col0; c0 < col0 + half; c0 += batch) {
           uint32_t v[kRBatch];
 #pragma unroll
           for (int c = 0; c < kRBatch; c += 16)
@@ -711,12 +725,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // every partial destined to this CTA has landed (bounded wait)
-    const bool got = !epi || __all_sync(0xffffffffu, ptx::mbar_wait(red_bar, 0));
+    const bool got = !red || __all_sync(0xffffffffu, ptx::mbar_wait(red_bar, 0));
     if (!got) report(kStatusEpilogue);
     // (the block runs whether or not the wait succeeded: its named barrier
-    // needs all four epilogue warps; a timeout is reported, the values are
+    // needs all the reducing warps; a timeout is reported, the values are
     // then garbage)
-    if (epi) {
+    if (red) {
       // sum into f16/bf16, stage [slice tokens][128 rows] in shared memory
       // (after the receive buffer), then store y with 16-byte vectors
       const int t = t_first;
@@ -724,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       AT* stage_y = reinterpret_cast<AT*>(gbase + (split - 1) * slice * kBM * 4);
       const float lb = layer_bias && n0 + r < N ? Act<AT>::to_f32(layer_bias[n0 + r]) : 0.0f;
 #pragma unroll 1
-      for (int c0 = 0; c0 < slice; c0 += batch) {
+      for (int c0 = col0; c0 < col0 + half; c0 += batch) {
         uint32_t v[kRBatch];
 #pragma unroll
         for (int c = 0; c < kRBatch; c += 16)
@@ -769,28 +783,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // the four epilogue warps' rows are all staged (the same branch for
-      // all four: y_f32 is a kernel argument)
+      // every reducing warp's columns are staged (the same branch for all of
+      // them: y_f32 is a kernel argument)
       if (!y_f32) {
-      asm volatile("bar.sync 2, 128;" ::: "memory");
-      const int et = threadIdx.x - (2 + kDequantWarps) * 32;  // 0..127
-      const bool vec = N % 8 == 0 && n0 + kBM <= N &&
-                       reinterpret_cast<uintptr_t>(y) % 16 == 0;
-      if (vec) {
-        // 16 chunks of 8 rows per token
+        const int n_red = 128 * parts;  // threads of the reducing warps
+        if (parts == 2)
+          asm volatile("bar.sync 2, 256;" ::: "memory");
+        else
+          asm volatile("bar.sync 2, 128;" ::: "memory");
+        const int et = part * 128 + quarter * 32 + lane;  // 0 .. n_red-1
+        const bool vec = N % 8 == 0 && n0 + kBM <= N &&
+                         reinterpret_cast<uintptr_t>(y) % 16 == 0;
+        if (vec) {
+          // 16 chunks of 8 rows per token
 #pragma unroll 1
-        for (int c = et; c < slice * 16; c += 128) {
-          const int mm = c >> 4, n8 = (c & 15) * 8;
-          if (m0 + mm < M)
-            *reinterpret_cast<uint4*>(y + int64_t(m0 + mm) * N + n0 + n8) =
-                *reinterpret_cast<const uint4*>(stage_y + mm * kBM + n8);
+          for (int c = et; c < slice * 16; c += n_red) {
+            const int mm = c >> 4, n8 = (c & 15) * 8;
+            if (m0 + mm < M)
+              *reinterpret_cast<uint4*>(y + int64_t(m0 + mm) * N + n0 + n8) =
+                  *reinterpret_cast<const uint4*>(stage_y + mm * kBM + n8);
+          }
+        } else {
+          const int n = n0 + r;
+          if (n < N)
+            for (int mm = col0; mm < col0 + half; ++mm)
+              if (m0 + mm < M) y[int64_t(m0 + mm) * N + n] = stage_y[mm * kBM + r];
         }
-      } else {
-        const int n = n0 + r;
-        if (n < N)
-          for (int mm = 0; mm < slice; ++mm)
-            if (m0 + mm < M) y[int64_t(m0 + mm) * N + n] = stage_y[mm * kBM + r];
-      }
       }
     }
     // no CTA leaves while another may still be writing into it
