@@ -199,3 +199,13 @@ def test_qmv_split_choice(L, monkeypatch):
     monkeypatch.setenv("QLIN_QMV_SPLIT", "4")
     assert f(300, 512, 4, 152) == 4          # 256-byte rows: 64 bytes a CTA
     assert f(3, 192, 4, 152) == 1            # 96-byte rows do not split in 4
+
+
+def test_qmv_rejects_k_beyond_the_staged_x(L, monkeypatch):
+    """qmv keeps x in shared memory as f32: a K whose x cannot fit beside the
+    ring is refused on the host (no launch), unless a split of K leaves each
+    CTA a slice that fits."""
+    monkeypatch.setenv("QLIN_QMV_SPLIT", "1")
+    assert _qmv(L, N=300, K=1 << 17, bits=8) == UNSUPPORTED
+    assert b"too large" in L.qlin_last_error()
+    assert _qmv(L, M=4, N=300, K=1 << 15, bits=8) == UNSUPPORTED

@@ -216,6 +216,25 @@ def test_qmv_split_k_factors(dev, qmv_split, split, m, n, k, bits, dt):
     assert q.device_status() == 0
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("split", [None, 1])
+def test_qmv_longest_k(dev, qmv_split, bits, split):
+    """M = 1 at K = 32768, near the largest K whose f32 x fits in shared memory
+    beside the ring: split by the host's choice (8 CTAs a row block, each
+    staging an eighth of x) and forced whole (every CTA staging all of x)."""
+    m, n, k, dt = 1, 300, 32768, "f16"
+    if split:
+        qmv_split(split)
+    w, x, ref = case(8400 + bits, m, n, k, bits, dt)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    buf, y = guarded((m, n), TORCH_DT[dt], dev)
+    q.qmv(x.to(dev), wq, sc, bi, bits, out=y)
+    torch.cuda.synchronize()
+    assert canaries_intact(buf)
+    assert_within_tolerance(y, ref, f"qmv K={k} b={bits} split={split}")
+    assert q.device_status() == 0
+
+
 def test_qmv_split_k_as_dependent_launch(dev):
     """A split-K qmv (a cluster per row block) launched as a programmatic
     dependent launch after the kernel that writes its input gives what a plain
