@@ -9,26 +9,29 @@
 // "The blocker (measured)").
 //
 // Orientation ("swap AB"): the MMA's M dimension is 128 weight rows and its N
-// dimension is a tile of BN = 16..256 tokens (the MMA takes about the same
-// time for every N up to 256, so the tile may be wider than the batch; rows
-// past M are zero-filled by the TMA).
+// dimension is a tile of BN = 16..256 tokens (a stage costs about the same
+// for every N up to 256, since the issuing thread's per-stage latency, not
+// the tensor pipe, sets it; so the tile may be wider than the batch, rows
+// past M being zero-filled by the TMA).
 //   D[n][m] (TMEM, f32) += W_hat[n][k] (TMEM, A operand) * x[m][k] (smem, B)
 //
 // Persistent CTAs (one per SM) walk 128 x BN output tiles, or, when the tiles
 // are too few for the SMs, a cluster of 2 or 4 CTAs shares each tile, each
 // CTA taking a slice of K, and the partial accumulators are summed through
-// distributed shared memory at the end.  The K loop runs in stages of one
+// distributed shared memory at the end (by the epilogue warps and the first
+// dequantising warpgroup, idle by then).  The K loop runs in stages of one
 // group (64 k) through a ring of shared-memory stages and, with the same
 // index, of TMEM A slots:
 //   warp 0       TMA producer: x tile [BN x 64] (128-byte swizzle), packed
 //                tile [128 rows x 64 codes] (32/64-byte swizzle) and, when the
 //                scale rows are 16-byte aligned, the 8-group scale and bias
 //                boxes holding the stage's group.
-//   warp 1       TMEM allocator and MMA issuer (one thread): 4 MMAs of K=16
-//                per stage (A from the stage's TMEM slot, B = x from shared
-//                memory) into a TMEM accumulator (two, alternating by tile,
-//                when BN <= 128), tcgen05.commit to free the stage / hand the
-//                tile over.
+//   warp 1       TMEM allocator and MMA issuer (one thread): per stage one
+//                wait, for the stage's A slot (its dequantisers waited for
+//                the stage's TMA bytes first), then 4 MMAs of K=16 (A from
+//                the stage's TMEM slot, B = x from shared memory) into a TMEM
+//                accumulator (two, alternating by tile, when BN <= 128), and
+//                tcgen05.commit to free the stage / hand the tile over.
 //   warps 2..9   two dequantising warpgroups taking stages in turn (thread =
 //                weight row = TMEM lane): unpack the row's 64 codes, w_hat =
 //                q*scale + bias in the operand type with one fused
