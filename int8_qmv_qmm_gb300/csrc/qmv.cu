@@ -23,7 +23,12 @@
 //
 // The per-chunk arithmetic, the lane-transposed x layout and the butterfly
 // reduction are in qmv_core.cuh.  Warp w computes rows w*R .. w*R+R-1 of each
-// stage; lanes take consecutive 16-byte chunks.  No global workspace.
+// stage; lanes take consecutive 16-byte chunks.  For one token on 2048-code
+// k-tiles with eight-row blocks, warp w instead takes rows 2(w%4), 2(w%4)+1
+// over half w/4 of every tile ("K halves"): each x value a lane loads from
+// shared memory then serves two rows, and the two warps of a row pair add
+// their sums through shared memory (3.4% off the decode step).  No global
+// workspace.
 //
 // Split of K.  When the row blocks are few and long (small N, long K), a
 // thread-block cluster of 2, 4 or 8 CTAs shares each row block: CTA c takes
@@ -70,14 +75,20 @@ struct Shape {
 
 // MODE 0: generic k-tiles, scales read from global memory; 1: generic k-tiles,
 // scales copied into the stage; 2: fixed 2048-code k-tiles with scales copied
-// (the fast path).  EPI: a linear layer's epilogue (bias, float32 output) is
-// applied; a separate instance, so the plain path's code is untouched.
+// (the fast path); 3: as 2, for one token (MT = 1) and 8-row blocks, each warp
+// taking two rows over one half of every k-tile (the rounds of its lanes), so
+// that every x value a lane loads serves two rows; the two warps of a row pair
+// add their sums through shared memory.  EPI: a linear layer's epilogue (bias,
+// float32 output) is applied; a separate instance, so the plain path's code is
+// untouched.
 template <int BITS, int MT, int R, typename AT, int MODE, bool EPI>
 __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
     const AT* __restrict__ x, const uint32_t* __restrict__ wq, const AT* __restrict__ scales,
     const AT* __restrict__ biases, AT* __restrict__ y, const Shape sh) {
   constexpr bool kScaleCopy = MODE != 0;
-  constexpr int kRB = kConsumerWarps * R;
+  constexpr bool kKH = MODE == 3;
+  static_assert(!kKH || (MT == 1 && R == 2), "K halves: one token, two rows per warp");
+  constexpr int kRB = kKH ? kConsumerWarps * R / 2 : kConsumerWarps * R;
   extern __shared__ __align__(16) uint8_t smem[];
   const int K = sh.K, N = sh.N;
   const int row_bytes = K * BITS / 8;
@@ -95,6 +106,10 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
   const uint32_t ring_u32 = ptx::smem_u32(ring);
   const uint32_t full0 = ptx::smem_u32(bars), empty0 = full0 + 8u * sh.stages;
   float* red = reinterpret_cast<float*>(bars + 2 * sh.stages);
+  // (K halves) [2 buffers][4 row pairs][2 rows] partial sums, then a flag a
+  // consumer sets when one of its waits gave up
+  float* kh_red = red;
+  volatile int* kh_abort = reinterpret_cast<volatile int*>(red + 16);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m0 = blockIdx.y * MT;
@@ -116,6 +131,7 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
       ptx::mbar_init(full0 + 8u * s, 1);
       ptx::mbar_init(empty0 + 8u * s, kConsumerWarps);
     }
+    if constexpr (kKH) *kh_abort = 0;
     ptx::fence_mbar_init();
   }
   __syncthreads();
@@ -209,10 +225,13 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
 
   const StageGeom geom{sh.kt_bytes, kt_groups, sh.rounds, gpr, N};
   float2* sbw = sb32 + warp * R * 32;
-  int s = 0;
+  // this warp's first row within a block, and (K halves) its half of the tile
+  const int w_row0 = kKH ? R * (warp & 3) : warp * R;
+  const int khalf = kKH ? warp >> 2 : 0;
+  int s = 0, kh_buf = 0;
   uint32_t round = 0;
   for (int blk = blk0; blk < sh.n_blocks; blk += blk_step) {
-    const int rb0 = blk * kRB + warp * R;  // this warp's first row
+    const int rb0 = blk * kRB + w_row0;  // this warp's first row
     float2 acc[R][MT];
 #pragma unroll
     for (int r = 0; r < R; ++r)
@@ -220,7 +239,25 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
       for (int mm = 0; mm < MT; ++mm) acc[r][mm] = make_float2(0.0f, 0.0f);
     bool failed = false;
     for (int kt = kt_lo; kt < kt_hi; ++kt) {
-      if (!ptx::mbar_wait(full0 + 8u * s, round & 1u)) {
+      if constexpr (kKH) {
+        // the warps of a row pair meet at a named barrier after every block:
+        // a warp whose wait gave up carries on without computing (and tells
+        // the others to stop waiting), so that its partner is never left
+        // waiting at that barrier
+        if (*kh_abort || !ptx::mbar_wait(full0 + 8u * s, round & 1u)) {
+          if (lane == 0 && !*kh_abort) {
+            atomicOr(&g_qmv_status, 2u);
+            *kh_abort = 1;
+          }
+          __syncwarp();
+          failed = true;
+          if (++s == sh.stages) {
+            s = 0;
+            ++round;
+          }
+          continue;
+        }
+      } else if (!ptx::mbar_wait(full0 + 8u * s, round & 1u)) {
         if (lane == 0) atomicOr(&g_qmv_status, 2u);
         // no CTA-wide barrier follows: leaving is safe, except that a split
         // CTA still takes part in the cluster barriers below
@@ -229,7 +266,17 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
         break;
       }
       const uint8_t* stage = ring + size_t(s) * sh.stage_bytes;
-      if constexpr (MODE == 2) {
+      if constexpr (kKH) {
+        constexpr int kHalfRounds = FixedTile<BITS>::kRounds / 2;
+        stage_scales_f32<BITS, R, AT>(stage, kRB, w_row0, sbw, lane);
+        if (khalf == 0)
+          accumulate_fixed<BITS, MT, R, AT, 0, kHalfRounds>(stage, w_row0, kt - kt_lo, sbw, xs,
+                                                            xs_m, xsum, sh.rounds * 32, lane,
+                                                            acc);
+        else
+          accumulate_fixed<BITS, MT, R, AT, kHalfRounds, kHalfRounds>(
+              stage, w_row0, kt - kt_lo, sbw, xs, xs_m, xsum, sh.rounds * 32, lane, acc);
+      } else if constexpr (MODE == 2) {
         stage_scales_f32<BITS, R, AT>(stage, kRB, warp * R, sbw, lane);
         accumulate_fixed<BITS, MT, R, AT>(stage, warp * R, kt - kt_lo, sbw, xs, xs_m, xsum,
                                           sh.rounds * 32, lane, acc);
@@ -246,6 +293,26 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
     }
     const AT* lbias = EPI ? static_cast<const AT*>(sh.ep.bias) : nullptr;
     const bool yf32 = EPI && sh.ep.y_f32 != 0;
+    if constexpr (kKH) {
+      // the half-1 warp of the pair hands its row sums to the half-0 warp,
+      // which adds them to its own (half 0 first) and stores the rows;
+      // two buffers by block parity, so a warp a block ahead never
+      // overwrites sums its partner has not read
+      using RS = RowSums<MT, R>;
+      float total = RS::reduce(acc, lane);
+      const int vi = RS::value_index(lane);
+      float* pr = kh_red + (kh_buf * 4 + (warp & 3)) * R;
+      if (khalf == 1 && RS::owner(lane)) pr[vi] = total;
+      asm volatile("bar.sync %0, 64;" ::"r"(3 + (warp & 3)) : "memory");
+      if (khalf == 0) {
+        total += pr[vi];
+        const int row = rb0 + vi;
+        if (RS::owner(lane) && row < N && !failed && !*kh_abort)
+          store_value<AT>(total, row, m0, static_cast<void*>(y), N, lbias, yf32);
+      }
+      kh_buf ^= 1;
+      continue;
+    }
     if (split == 1) {
       store_rows<MT, R, AT>(acc, lane, rb0, m0, N, sh.M, static_cast<void*>(y), N, lbias, yf32);
       continue;
@@ -279,9 +346,10 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
 // ------------------------------------------------------------------- host
 size_t smem_for(const Shape& sh, int MT, int R, int bits) {
   const int cw = 128 / bits;
+  // ... + the split-K receive buffer, or 16 partial sums and a flag (K halves)
   return size_t(sh.stages) * sh.stage_bytes + size_t(MT) * sh.rounds * 32 * cw * 4 +
          size_t(MT) * sh.rounds * 32 * 8 + size_t(kConsumerWarps) * R * 32 * 8 +
-         size_t(sh.stages) * 16 + size_t(sh.split - 1) * kConsumerWarps * R * MT * 4;
+         size_t(sh.stages) * 16 + size_t(sh.split - 1) * kConsumerWarps * R * MT * 4 + 80;
 }
 
 template <int BITS, int MT, int R, typename AT, int MODE, bool EPI>
@@ -449,15 +517,26 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
     const int v = std::atoi(env);
     if (v >= 16 && v <= 200) ring_kb = v;
   }
+  // one token on fixed k-tiles with one row per warp: the K-halves layout
+  // (mode 3: two rows per warp, each over half of every tile) instead, unless
+  // QLIN_QMV_KH=0 (tuning)
+  bool kh = MT == 1 && mode == 2 && R == 1 && split == 1;
+  if (const char* env = std::getenv("QLIN_QMV_KH")) kh = kh && std::atoi(env) != 0;
+  const int r_smem = kh ? 2 : R;  // rows per warp that size the scale pairs
   sh.stages = std::max(2, std::min(8, (ring_kb * 1024) / sh.stage_bytes));
-  size_t smem = smem_for(sh, MT, R, BITS);
+  size_t smem = smem_for(sh, MT, r_smem, BITS);
   while (sh.stages > 2 && smem > 110 * 1024) {
     --sh.stages;
-    smem = smem_for(sh, MT, R, BITS);
+    smem = smem_for(sh, MT, r_smem, BITS);
   }
   if (smem > 220 * 1024)
     return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmv: K=%d too large for the staged x", sh.K);
   const bool epi = sh.ep.bias != nullptr || sh.ep.y_f32;
+  if constexpr (MT == 1) {
+    if (kh)
+      return epi ? launch_t<BITS, 1, 2, AT, 3, true>(x, wq, scales, biases, y, sh, smem, st)
+                 : launch_t<BITS, 1, 2, AT, 3, false>(x, wq, scales, biases, y, sh, smem, st);
+  }
 #define QLIN_QMV_LAUNCH(RR, E)                                                                  \
   return mode == 2   ? launch_t<BITS, MT, RR, AT, 2, E>(x, wq, scales, biases, y, sh, smem, st)  \
          : mode == 1 ? launch_t<BITS, MT, RR, AT, 1, E>(x, wq, scales, biases, y, sh, smem, st)  \

@@ -287,7 +287,9 @@ __device__ __forceinline__ void stage_scales_f32(const uint8_t* stage, int RB, i
 }
 
 // kt: the k-tile of the staged x (the packed tile is the stage itself).
-template <int BITS, int MT, int R, typename AT>
+// Rounds [I0, I0 + NI) of the tile (every round by default): a round is the
+// 32 consecutive chunks of a row that the warp's lanes take at once.
+template <int BITS, int MT, int R, typename AT, int I0 = 0, int NI = FixedTile<BITS>::kRounds>
 __device__ __forceinline__ void accumulate_fixed(const uint8_t* stage, int w0, int kt,
                                                  const float2* sb32, const float* xs, int xs_m,
                                                  const float2* xsum, int xsum_m, int lane,
@@ -302,7 +304,7 @@ __device__ __forceinline__ void accumulate_fixed(const uint8_t* stage, int w0, i
   const float2* xsl = xsum + kt * T::kChunks + lane;
   const float2* sbl = sb32 + (lane * kCW) / kGroup;
 #pragma unroll
-  for (int i = 0; i < T::kRounds; ++i) {
+  for (int i = I0; i < I0 + NI; ++i) {
     uint4 cw[R];
     float2 s2[R], b2[R];
 #pragma unroll

@@ -235,6 +235,26 @@ def test_qmv_longest_k(dev, qmv_split, bits, split):
     assert q.device_status() == 0
 
 
+@pytest.mark.parametrize("bits,dt", [(4, "f16"), (8, "bf16")])
+def test_qmv_k_halves_one_hot_exact(dev, bits, dt):
+    """M = 1 on fixed 2048-code k-tiles runs two rows per warp, each warp over
+    one half of every tile, the pair's sums added in shared memory.  With
+    x = e_k one half holds the only nonzero term and the other adds an exact
+    zero: the output is the reconstructed weight bit for bit."""
+    n = 1029
+    k = 4096 if bits == 4 else 2048     # row blocks too short for a split of K
+    assert q.lib().qlin_testing_qmv_split(n, k, bits, 152) == 1
+    w = S.weights_f32(81, n, k)
+    wq, sc, bi = _upload(dev, w, bits, dt)
+    w_hat = q.dequant(wq, sc, bi, bits)
+    for col in (0, 5, 1023, 1024, k // 2 - 1, k // 2, k - 65, k - 1):
+        x = torch.zeros((1, k), dtype=TORCH_DT[dt])
+        x[0, col] = 1
+        y = q.qmv(x.to(dev), wq, sc, bi, bits)
+        assert torch.equal(y[0].cpu(), w_hat[:, col].cpu()), col
+    assert q.device_status() == 0
+
+
 def test_qmv_split_k_as_dependent_launch(dev):
     """A split-K qmv (a cluster per row block) launched as a programmatic
     dependent launch after the kernel that writes its input gives what a plain
@@ -308,6 +328,7 @@ def test_linear_dispatches_both_paths(dev):
 
 @pytest.mark.parametrize("m,n,k,bits,dt", [
     (1, 300, 512, 4, "f16"), (3, 1029, 2048, 8, "bf16"),        # qmv
+    (1, 1029, 2048, 8, "bf16"),                                   # qmv, K halves
     (40, 301, 512, 4, "f16"), (600, 384, 512, 8, "bf16"),        # qmm
     (512, 2048, 8192, 4, "f16"), (32, 8192, 2048, 4, "bf16"),    # qmm, K split over a cluster
 ])
@@ -486,12 +507,17 @@ def test_qmv_chain_independent_links_match_oracle(dev, bits, dt):
 
 
 @pytest.mark.parametrize("bits,dt", [(8, "f16"), (4, "bf16")])
-def test_qmv_chain_matches_sequential_launches(dev, bits, dt):
+def test_qmv_chain_matches_sequential_launches(dev, bits, dt, monkeypatch):
     """A dependent chain (slices of earlier outputs, K not a multiple of 512 so
     scales come from global memory, K = 8192 split into k-tiles): each link's
     output is within the tolerance of the oracle's product of its actual input
     (an earlier link's output, as the chain read it), and equals qlin_qmv
-    launched on that input bit for bit.  The chain reruns bit for bit."""
+    launched on that input bit for bit, in the layout the chain shares with it
+    (rows per warp over whole k-tiles, no split of K across CTAs: the
+    K-halves layout and the split add the same terms in another order).  The
+    chain reruns bit for bit."""
+    monkeypatch.setenv("QLIN_QMV_KH", "0")
+    monkeypatch.setenv("QLIN_QMV_SPLIT", "1")
     specs = [(3072, 2048, bits, -1, 0), (2048, 2048, bits, 0, 0), (4160, 2048, bits, 1, 0),
              (2048, 4096, bits, 2, 64), (320, 2048, bits, 3, 0), (1000, 192, bits, 4, 128),
              (8192, 320, bits, 5, 8), (96, 8192, bits, 6, 0)]
