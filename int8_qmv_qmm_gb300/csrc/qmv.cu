@@ -76,9 +76,9 @@ struct Shape {
 // MODE 0: generic k-tiles, scales read from global memory; 1: generic k-tiles,
 // scales copied into the stage; 2: fixed 2048-code k-tiles with scales copied
 // (the fast path); 3: as 2, for one token (MT = 1) and 8-row blocks, each warp
-// taking two rows over one half of every k-tile (the rounds of its lanes), so
-// that every x value a lane loads serves two rows; the two warps of a row pair
-// add their sums through shared memory.  EPI: a linear layer's epilogue (bias,
+// taking R rows (2 or 4) over one R-th part of every k-tile (of the rounds of
+// its lanes), so that every x value a lane loads serves R rows; the R warps of
+// a row group add their sums through shared memory.  EPI: a linear layer's epilogue (bias,
 // float32 output) is applied; a separate instance, so the plain path's code is
 // untouched.
 template <int BITS, int MT, int R, typename AT, int MODE, bool EPI>
@@ -87,8 +87,12 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
     const AT* __restrict__ biases, AT* __restrict__ y, const Shape sh) {
   constexpr bool kScaleCopy = MODE != 0;
   constexpr bool kKH = MODE == 3;
-  static_assert(!kKH || (MT == 1 && R == 2), "K halves: one token, two rows per warp");
-  constexpr int kRB = kKH ? kConsumerWarps * R / 2 : kConsumerWarps * R;
+  static_assert(!kKH || (MT == 1 && (R == 2 || R == 4) &&
+                         FixedTile<BITS>::kRounds % R == 0),
+                "K parts: one token, R rows per warp over R parts of whole rounds");
+  constexpr int kRB = kKH ? kConsumerWarps : kConsumerWarps * R;
+  // (K parts) row groups of R rows, each shared by R warps
+  constexpr int kGroups = kKH ? kConsumerWarps / R : 1;
   extern __shared__ __align__(16) uint8_t smem[];
   const int K = sh.K, N = sh.N;
   const int row_bytes = K * BITS / 8;
@@ -106,10 +110,10 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
   const uint32_t ring_u32 = ptx::smem_u32(ring);
   const uint32_t full0 = ptx::smem_u32(bars), empty0 = full0 + 8u * sh.stages;
   float* red = reinterpret_cast<float*>(bars + 2 * sh.stages);
-  // (K halves) [2 buffers][4 row pairs][2 rows] partial sums, then a flag a
-  // consumer sets when one of its waits gave up
+  // (K parts) [2 buffers][row groups][R-1 parts][R rows] partial sums (at
+  // most 48 floats), then a flag a consumer sets when one of its waits gave up
   float* kh_red = red;
-  volatile int* kh_abort = reinterpret_cast<volatile int*>(red + 16);
+  volatile int* kh_abort = reinterpret_cast<volatile int*>(red + 48);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int m0 = blockIdx.y * MT;
@@ -225,9 +229,11 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
 
   const StageGeom geom{sh.kt_bytes, kt_groups, sh.rounds, gpr, N};
   float2* sbw = sb32 + warp * R * 32;
-  // this warp's first row within a block, and (K halves) its half of the tile
-  const int w_row0 = kKH ? R * (warp & 3) : warp * R;
-  const int khalf = kKH ? warp >> 2 : 0;
+  // this warp's first row within a block, and (K parts) its row group and
+  // its part of the tile
+  const int kh_group = kKH ? warp % kGroups : 0;
+  const int w_row0 = kKH ? R * kh_group : warp * R;
+  const int khalf = kKH ? warp / kGroups : 0;
   int s = 0, kh_buf = 0;
   uint32_t round = 0;
   for (int blk = blk0; blk < sh.n_blocks; blk += blk_step) {
@@ -267,15 +273,24 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
       }
       const uint8_t* stage = ring + size_t(s) * sh.stage_bytes;
       if constexpr (kKH) {
-        constexpr int kHalfRounds = FixedTile<BITS>::kRounds / 2;
+        constexpr int kPartRounds = FixedTile<BITS>::kRounds / R;
         stage_scales_f32<BITS, R, AT>(stage, kRB, w_row0, sbw, lane);
+        // (the part index selects compile-time round ranges)
         if (khalf == 0)
-          accumulate_fixed<BITS, MT, R, AT, 0, kHalfRounds>(stage, w_row0, kt - kt_lo, sbw, xs,
+          accumulate_fixed<BITS, MT, R, AT, 0, kPartRounds>(stage, w_row0, kt - kt_lo, sbw, xs,
                                                             xs_m, xsum, sh.rounds * 32, lane,
                                                             acc);
-        else
-          accumulate_fixed<BITS, MT, R, AT, kHalfRounds, kHalfRounds>(
+        else if (khalf == 1)
+          accumulate_fixed<BITS, MT, R, AT, kPartRounds, kPartRounds>(
               stage, w_row0, kt - kt_lo, sbw, xs, xs_m, xsum, sh.rounds * 32, lane, acc);
+        else if constexpr (R == 4) {
+          if (khalf == 2)
+            accumulate_fixed<BITS, MT, R, AT, 2 * kPartRounds, kPartRounds>(
+                stage, w_row0, kt - kt_lo, sbw, xs, xs_m, xsum, sh.rounds * 32, lane, acc);
+          else
+            accumulate_fixed<BITS, MT, R, AT, 3 * kPartRounds, kPartRounds>(
+                stage, w_row0, kt - kt_lo, sbw, xs, xs_m, xsum, sh.rounds * 32, lane, acc);
+        }
       } else if constexpr (MODE == 2) {
         stage_scales_f32<BITS, R, AT>(stage, kRB, warp * R, sbw, lane);
         accumulate_fixed<BITS, MT, R, AT>(stage, warp * R, kt - kt_lo, sbw, xs, xs_m, xsum,
@@ -294,18 +309,18 @@ __global__ void __launch_bounds__(kThreads, 2) qmv_kernel(
     const AT* lbias = EPI ? static_cast<const AT*>(sh.ep.bias) : nullptr;
     const bool yf32 = EPI && sh.ep.y_f32 != 0;
     if constexpr (kKH) {
-      // the half-1 warp of the pair hands its row sums to the half-0 warp,
-      // which adds them to its own (half 0 first) and stores the rows;
-      // two buffers by block parity, so a warp a block ahead never
-      // overwrites sums its partner has not read
+      // the warps of parts 1.. of a row group hand their row sums to the
+      // part-0 warp, which adds them to its own in part order and stores the
+      // rows; two buffers by block parity, so a warp a block ahead never
+      // overwrites sums not yet read
       using RS = RowSums<MT, R>;
       float total = RS::reduce(acc, lane);
       const int vi = RS::value_index(lane);
-      float* pr = kh_red + (kh_buf * 4 + (warp & 3)) * R;
-      if (khalf == 1 && RS::owner(lane)) pr[vi] = total;
-      asm volatile("bar.sync %0, 64;" ::"r"(3 + (warp & 3)) : "memory");
+      float* pr = kh_red + (kh_buf * kGroups + kh_group) * (R - 1) * R;
+      if (khalf > 0 && RS::owner(lane)) pr[(khalf - 1) * R + vi] = total;
+      asm volatile("bar.sync %0, %1;" ::"r"(3 + kh_group), "n"(32 * R) : "memory");
       if (khalf == 0) {
-        total += pr[vi];
+        for (int p = 0; p < R - 1; ++p) total += pr[p * R + vi];
         const int row = rb0 + vi;
         if (RS::owner(lane) && row < N && !failed && !*kh_abort)
           store_value<AT>(total, row, m0, static_cast<void*>(y), N, lbias, yf32);
@@ -349,7 +364,7 @@ size_t smem_for(const Shape& sh, int MT, int R, int bits) {
   // ... + the split-K receive buffer, or 16 partial sums and a flag (K halves)
   return size_t(sh.stages) * sh.stage_bytes + size_t(MT) * sh.rounds * 32 * cw * 4 +
          size_t(MT) * sh.rounds * 32 * 8 + size_t(kConsumerWarps) * R * 32 * 8 +
-         size_t(sh.stages) * 16 + size_t(sh.split - 1) * kConsumerWarps * R * MT * 4 + 80;
+         size_t(sh.stages) * 16 + size_t(sh.split - 1) * kConsumerWarps * R * MT * 4 + 208;
 }
 
 template <int BITS, int MT, int R, typename AT, int MODE, bool EPI>
@@ -517,12 +532,17 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
     const int v = std::atoi(env);
     if (v >= 16 && v <= 200) ring_kb = v;
   }
-  // one token on fixed k-tiles with one row per warp: the K-halves layout
-  // (mode 3: two rows per warp, each over half of every tile) instead, unless
-  // QLIN_QMV_KH=0 (tuning)
-  bool kh = MT == 1 && mode == 2 && R == 1 && split == 1;
-  if (const char* env = std::getenv("QLIN_QMV_KH")) kh = kh && std::atoi(env) != 0;
-  const int r_smem = kh ? 2 : R;  // rows per warp that size the scale pairs
+  // one token on fixed k-tiles with one row per warp: the K-parts layout
+  // (mode 3: R rows per warp, each over an R-th of every tile) instead, with
+  // R = 2 (decode step: 358 us against 370 without; R = 4, possible where a
+  // tile has 4 rounds, measured 367).  QLIN_QMV_KH (0, 2 or 4) overrides it,
+  // for tuning.
+  int kh = (MT == 1 && mode == 2 && R == 1 && split == 1) ? 2 : 0;
+  if (const char* env = std::getenv("QLIN_QMV_KH")) {
+    const int v = std::atoi(env);
+    if (v == 0 || v == 2 || (v == 4 && FixedTile<BITS>::kRounds % 4 == 0)) kh = kh ? v : 0;
+  }
+  const int r_smem = kh ? kh : R;  // rows per warp that size the scale pairs
   sh.stages = std::max(2, std::min(8, (ring_kb * 1024) / sh.stage_bytes));
   size_t smem = smem_for(sh, MT, r_smem, BITS);
   while (sh.stages > 2 && smem > 110 * 1024) {
@@ -533,7 +553,12 @@ qlin_status dispatch_mt(const void* x, const uint32_t* wq, const void* scales,
     return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmv: K=%d too large for the staged x", sh.K);
   const bool epi = sh.ep.bias != nullptr || sh.ep.y_f32;
   if constexpr (MT == 1) {
-    if (kh)
+    if constexpr (FixedTile<BITS>::kRounds % 4 == 0) {
+      if (kh == 4)
+        return epi ? launch_t<BITS, 1, 4, AT, 3, true>(x, wq, scales, biases, y, sh, smem, st)
+                   : launch_t<BITS, 1, 4, AT, 3, false>(x, wq, scales, biases, y, sh, smem, st);
+    }
+    if (kh == 2)
       return epi ? launch_t<BITS, 1, 2, AT, 3, true>(x, wq, scales, biases, y, sh, smem, st)
                  : launch_t<BITS, 1, 2, AT, 3, false>(x, wq, scales, biases, y, sh, smem, st);
   }
