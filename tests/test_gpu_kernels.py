@@ -235,12 +235,15 @@ def test_qmv_longest_k(dev, qmv_split, bits, split):
     assert q.device_status() == 0
 
 
-@pytest.mark.parametrize("bits,dt", [(4, "f16"), (8, "bf16")])
-def test_qmv_k_halves_one_hot_exact(dev, bits, dt):
-    """M = 1 on fixed 2048-code k-tiles runs two rows per warp, each warp over
-    one half of every tile, the pair's sums added in shared memory.  With
-    x = e_k one half holds the only nonzero term and the other adds an exact
-    zero: the output is the reconstructed weight bit for bit."""
+@pytest.mark.parametrize("bits,dt,parts", [(4, "f16", 2), (8, "bf16", 2), (8, "f16", 4)])
+def test_qmv_k_parts_one_hot_exact(dev, monkeypatch, bits, dt, parts):
+    """M = 1 on fixed 2048-code k-tiles runs R rows per warp, each warp over
+    one R-th of every tile (R = 2 by default, 4 as a tuning option), the row
+    group's sums added in shared memory.  With x = e_k one part holds the only
+    nonzero term and the others add exact zeros: the output is the
+    reconstructed weight bit for bit; and random x stays within the
+    tolerance."""
+    monkeypatch.setenv("QLIN_QMV_KH", str(parts))
     n = 1029
     k = 4096 if bits == 4 else 2048     # row blocks too short for a split of K
     assert q.lib().qlin_testing_qmv_split(n, k, bits, 152) == 1
@@ -252,6 +255,9 @@ def test_qmv_k_halves_one_hot_exact(dev, bits, dt):
         x[0, col] = 1
         y = q.qmv(x.to(dev), wq, sc, bi, bits)
         assert torch.equal(y[0].cpu(), w_hat[:, col].cpu()), col
+    _, xr, ref = case(8500 + parts, 1, n, k, bits, dt)
+    ref = O.linear_ref(xr.float().numpy().astype(np.float64), w, bits, 64, dt)
+    assert_within_tolerance(q.qmv(xr.to(dev), wq, sc, bi, bits), ref, f"K parts {parts}")
     assert q.device_status() == 0
 
 
