@@ -447,11 +447,17 @@ def time_qmm(q, device, peaks):
         xs, wqs, scs, bis, ys = (_replicas(t, sets) for t in (x, wq, sc, bi, y))
         t = time_rotating(lambda i: q.qmm(xs[i], wqs[i], scs[i], bis[i], bits, out=ys[i]),
                           sets, device)
+        # the same launches as programmatic dependent launches (qlin_qmm_ex), as
+        # a chain of prefill linears would issue them: each kernel's set-up
+        # overlaps the previous one's tail
+        t_pdl = time_rotating(lambda i: q.qmm(xs[i], wqs[i], scs[i], bis[i], bits, out=ys[i],
+                                              overlap_previous=i > 0), sets, device)
         del xs, wqs, scs, bis, ys
         t_iso = time_flushed(lambda: q.qmm(x, wq, sc, bi, bits, out=y), device, flush, reps=30)
         flops = 2.0 * m * n * k
         rows.append({"m": m, "n": n, "k": k, "bits": bits, "us": t * 1e6,
                      "tflops": flops / t / 1e12, "rotating_sets": sets,
+                     "overlapped_us": t_pdl * 1e6, "overlapped_tflops": flops / t_pdl / 1e12,
                      "isolated_flushed_us": t_iso * 1e6})
     del flush
     torch.cuda.empty_cache()
@@ -461,8 +467,11 @@ def time_qmm(q, device, peaks):
     return {
         "tflops_mean": mean, "tflops_best": best, "tflops_worst": worst, "cases": rows,
         "timing": "us = GPU time per launch, launches back to back over rotating operand "
-                  "copies (2.5x L2) in one CUDA graph; isolated_flushed_us = median of single "
+                  "copies (2.5x L2) in one CUDA graph (the roofline uses these); overlapped_us "
+                  "= the same as programmatic dependent launches (qlin_qmm_ex), as a chain "
+                  "of prefill linears issues them; isolated_flushed_us = median of single "
                   "launches after an L2 flush (event overhead included)",
+        "overlapped_tflops_mean": statistics.mean(r["overlapped_tflops"] for r in rows),
         "roofline": {"bound": "tensor", "achieved": mean, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": mean / peaks["bf16_tflops"],
                      "frac_worst": worst / peaks["bf16_tflops"],
