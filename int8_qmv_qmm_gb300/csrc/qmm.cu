@@ -143,14 +143,16 @@ struct OperandSplit {
 // TMEM: kDBufs accumulators of BN columns, then one slot of SPLIT x 32 columns
 // per ring stage holding the stage's dequantised A tile(s) (128 lanes x 64
 // 16-bit values each).
-template <int BITS, int BN, int SPLIT>
+// BOX: the stage holds the scale and bias boxes (they come by TMA); without
+// them a stage is 4 KB smaller, which can make room for one more stage.
+template <int BITS, int BN, int SPLIT, bool BOX>
 struct Layout {
   static constexpr int kXBytes = BN * kBK * 2;           // x tile, 128-byte rows
   static constexpr int kWBytes = Geo<BITS>::kPackedBytes;
   static constexpr int kSBytes = 2 * kBM * 16;           // 8 groups of scales + of biases
   static constexpr int kWOff = round_up(kXBytes, 1024);
   static constexpr int kSOff = kWOff + round_up(kWBytes, 1024);
-  static constexpr int kStageBytes = kSOff + round_up(kSBytes, 1024);
+  static constexpr int kStageBytes = kSOff + (BOX ? round_up(kSBytes, 1024) : 0);
   static constexpr int kTxBytes = kXBytes + kWBytes;
   // two accumulators (the epilogue of a tile overlaps the next tile's K loop)
   // unless they would leave TMEM too few A slots
@@ -380,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                int M, int N, int K, int stages, int tmem_cols, int split,
                const AT* __restrict__ layer_bias, int y_f32) {
   constexpr int kSplit = OperandSplit<AT>::value;
-  using L = Layout<BITS, BN, kSplit>;
+  using L = Layout<BITS, BN, kSplit, SCALE_TMA>;
   using G = Geo<BITS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
@@ -864,11 +866,11 @@ qlin_status make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, 
   return QLIN_OK;
 }
 
-template <int BITS, typename AT, int BN>
-qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, const void* biases,
-                      void* y, int64_t M, int64_t N, int64_t K, int split, const Epilogue& ep,
-                      unsigned flags, cudaStream_t st) {
-  using L = Layout<BITS, BN, OperandSplit<AT>::value>;
+template <int BITS, typename AT, int BN, bool SCALE_TMA>
+qlin_status launch_layout(const void* x, const uint32_t* wq, const void* scales,
+                          const void* biases, void* y, int64_t M, int64_t N, int64_t K, int split,
+                          const Epilogue& ep, unsigned flags, cudaStream_t st) {
+  using L = Layout<BITS, BN, OperandSplit<AT>::value, SCALE_TMA>;
   constexpr int kMaxSmem = 227 * 1024;
   constexpr int kBarBytes = 512;
   // (kDequantGroups + 2) barriers per stage (at most 8), two pairs of
@@ -907,18 +909,8 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
                Geo<BITS>::kWordsPerGroup, kBM,
                BITS == 4 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
   if (s != QLIN_OK) return s;
-  // scales/biases by TMA in boxes of 8 groups x 128 rows (needs 16-byte
-  // rows), of which a stage uses one group.  For rows of at most 32 groups
-  // (K <= 2048) the dequantising threads read their row's scale and bias from
-  // global memory instead (L1 holds the row's 64 bytes of each for all its
-  // stages; the loads are issued before the stage's barrier wait): 2-6%
-  // faster there (8192 x 2048 at M = 2048: 62.8 -> 61.1 us at 4 bits, 62.3 ->
-  // 58.8 at 8 bits), while at K = 8192 the boxes are 3-9% faster.
-  const uint64_t gpr = uint64_t(K) / kGroup;
-  const bool scale_tma = gpr > 32 && gpr % 8 == 0 &&
-                         reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
-                         reinterpret_cast<uintptr_t>(biases) % 16 == 0;
-  if (scale_tma) {
+  if constexpr (SCALE_TMA) {
+    const uint64_t gpr = uint64_t(K) / kGroup;
     if ((s = make_map(&tm_s, adt, scales, gpr, uint64_t(N), gpr * 2, 8, kBM,
                       CU_TENSOR_MAP_SWIZZLE_NONE)) != QLIN_OK)
       return s;
@@ -930,15 +922,15 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
     tm_b = tm_x;
   }
 
-  auto kern = scale_tma ? qmm_kernel<BITS, AT, BN, true> : qmm_kernel<BITS, AT, BN, false>;
-  static int attr_dev[2] = {-1, -1};
+  auto kern = qmm_kernel<BITS, AT, BN, SCALE_TMA>;
+  static int attr_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (attr_dev[scale_tma] != dev) {
+  if (attr_dev != dev) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem) !=
         cudaSuccess)
       return check_launch("qlin_qmm: cudaFuncSetAttribute");
-    attr_dev[scale_tma] = dev;
+    attr_dev = dev;
   }
   const int64_t tiles = ((N + kBM - 1) / kBM) * ((M + BN - 1) / BN);
   if (tiles > (int64_t(1) << 30)) return fail(QLIN_ERR_UNSUPPORTED, "qlin_qmm: too many tiles");
@@ -974,6 +966,29 @@ qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, con
     return fail(QLIN_ERR_CUDA, "qmm_kernel launch: %s", cudaGetErrorString(e));
   }
   return check_launch("qmm_kernel");
+}
+
+// Scales and biases by TMA boxes of 8 groups x 128 rows (needs 16-byte
+// rows), of which a stage uses one group, for rows of more than 32 groups.
+// For rows of at most 32 groups (K <= 2048) the dequantising threads read
+// their row's scale and bias from global memory instead (L1 holds the row's
+// 64 bytes of each for all its stages; the loads are issued before the
+// stage's barrier wait), and the stages, 4 KB smaller without the boxes, make
+// room for a sixth at 4 bits: 2-6% faster there (8192 x 2048 at M = 2048:
+// 62.8 -> 61.1 us at 4 bits, 62.3 -> 58.8 at 8 bits), while at K = 8192 the
+// boxes are 3-9% faster.
+template <int BITS, typename AT, int BN>
+qlin_status launch_bn(const void* x, const uint32_t* wq, const void* scales, const void* biases,
+                      void* y, int64_t M, int64_t N, int64_t K, int split, const Epilogue& ep,
+                      unsigned flags, cudaStream_t st) {
+  const uint64_t gpr = uint64_t(K) / kGroup;
+  const bool scale_tma = gpr > 32 && gpr % 8 == 0 &&
+                         reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(biases) % 16 == 0;
+  return scale_tma ? launch_layout<BITS, AT, BN, true>(x, wq, scales, biases, y, M, N, K, split,
+                                                       ep, flags, st)
+                   : launch_layout<BITS, AT, BN, false>(x, wq, scales, biases, y, M, N, K,
+                                                        split, ep, flags, st);
 }
 
 template <int BITS, typename AT>
